@@ -1,0 +1,145 @@
+"""Seeded synthetic inputs for the CODA GEMM-epilogue workloads.
+
+This module is the only code shared by the CUDA path's tests/bench and the
+oracle. It draws random tensors and encodes them as bfloat16 bit patterns; it
+holds none of the method's arithmetic (no GEMM, normalisation, activation,
+rotation or loss).
+
+Recipe (the same for every workload):
+  * ``numpy.random.Generator(PCG64)`` seeded from ``SeedSequence(seed)``;
+    ``seed`` defaults to 0. One ``spawn`` child per tensor, in the order the
+    workload lists its tensors, so a forward tensor is identical whether or not
+    the backward tensors are requested.
+  * Draw float32 standard normals, scale (and shift) in float32, then round
+    to bfloat16 with round-to-nearest-even. The result is returned as
+    ``uint16`` bit patterns so every consumer reads the same bytes.
+  * Labels are int32, uniform in ``[0, V)``.
+
+Distributions (weights ~ N(0, 1/fan_in), activations ~ N(0, 1),
+gamma ~ 1 + 0.1 N(0, 1)) follow the workload statements that accompany the
+CODA paper's kernel table (GEMM+RoPE QKV projection, GEMM+SwiGLU up-projection,
+GEMM-RMSNorm-GEMM, LM-head GEMM + cross-entropy).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "f32_to_bf16_bits",
+    "normal_bf16",
+    "rms_chain",
+    "rope_problem",
+    "swiglu_problem",
+    "ce_problem",
+    "WORKLOADS",
+]
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round-to-nearest-even); return uint16 bits.
+
+    Inputs here are finite normals, so NaN/Inf handling is not needed; it is
+    still guarded so a NaN stays a NaN.
+    """
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    rounded = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    out = rounded.astype(np.uint16)
+    nan = np.isnan(a)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def _children(seed: int, n: int):
+    return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(n)]
+
+
+def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
+    """bf16 bits of ``mean + std * N(0, 1)`` drawn in float32."""
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    if mean != 0.0:
+        x += np.float32(mean)
+    return f32_to_bf16_bits(x)
+
+
+def rms_chain(M: int, K: int, d: int, N2: int, seed: int = 0, bwd_K: int | None = None) -> dict:
+    """GEMM -> residual add -> RMSNorm -> GEMM problem.
+
+    Tensors, in spawn order: x[M,K] ~ N(0,1), W0[K,d] ~ N(0,1/K),
+    z[M,d] ~ N(0,1), gamma[d] ~ 1 + 0.1 N(0,1), W1[d,N2] ~ N(0,1/d), and for
+    the backward stand-in GEMM that produces the output gradient dY = dO Wn:
+    dO[M,bwd_K] ~ N(0,1), Wn[bwd_K,N2] ~ N(0,1/bwd_K).
+    """
+    g = _children(seed, 7)
+    out = {
+        "x": normal_bf16(g[0], (M, K)),
+        "W0": normal_bf16(g[1], (K, d), std=1.0 / np.sqrt(K)),
+        "z": normal_bf16(g[2], (M, d)),
+        "gamma": normal_bf16(g[3], (d,), std=0.1, mean=1.0),
+        "W1": normal_bf16(g[4], (d, N2), std=1.0 / np.sqrt(d)),
+    }
+    if bwd_K is not None:
+        out["dO"] = normal_bf16(g[5], (M, bwd_K))
+        out["Wn"] = normal_bf16(g[6], (bwd_K, N2), std=1.0 / np.sqrt(bwd_K))
+    return out
+
+
+def rope_problem(M: int, K: int, N3: int, seed: int = 0, with_bwd: bool = True) -> dict:
+    """QKV projection X[M,K] ~ N(0,1) times W[K,N3] ~ N(0,1/K).
+
+    Backward stand-in operands of the same shapes: A[M,K] ~ N(0,1),
+    B[K,N3] ~ N(0,1/K) (their product plays the gradient of the rotated
+    output).
+    """
+    g = _children(seed, 4)
+    out = {
+        "X": normal_bf16(g[0], (M, K)),
+        "W": normal_bf16(g[1], (K, N3), std=1.0 / np.sqrt(K)),
+    }
+    if with_bwd:
+        out["A"] = normal_bf16(g[2], (M, K))
+        out["B"] = normal_bf16(g[3], (K, N3), std=1.0 / np.sqrt(K))
+    return out
+
+
+def swiglu_problem(M: int, K: int, F: int, seed: int = 0, with_bwd: bool = True) -> dict:
+    """MLP up-projection X[M,K] ~ N(0,1) times gate/up-interleaved Wgu[K,2F] ~ N(0,1/K).
+
+    Backward: dY[M,K] ~ N(0,1) (gradient of the down-projection output) and the
+    down-projection weight Wd[F,K] ~ N(0,1/F), stored [F, K].
+    """
+    g = _children(seed, 4)
+    out = {
+        "X": normal_bf16(g[0], (M, K)),
+        "Wgu": normal_bf16(g[1], (K, 2 * F), std=1.0 / np.sqrt(K)),
+    }
+    if with_bwd:
+        out["dY"] = normal_bf16(g[2], (M, K))
+        out["Wd"] = normal_bf16(g[3], (F, K), std=1.0 / np.sqrt(F))
+    return out
+
+
+def ce_problem(M: int, K: int, V: int, seed: int = 0) -> dict:
+    """LM head H[M,K] ~ N(0,1) times W[K,V] ~ N(0,1/K); labels int32 uniform in [0,V)."""
+    g = _children(seed, 3)
+    return {
+        "H": normal_bf16(g[0], (M, K)),
+        "W": normal_bf16(g[1], (K, V), std=1.0 / np.sqrt(K)),
+        "labels": g[2].integers(0, V, size=(M,), dtype=np.int32),
+    }
+
+
+# The five workloads, by name, with their full sizes.
+WORKLOADS = {
+    "rmsnorm_chain_tiny": dict(kind="rms_chain", M=256, K=512, d=512, N2=512, eps=1e-6),
+    "rope_qkv_4096": dict(kind="rope", M=4096, K=4096, N3=12288, head_dim=128, theta=10000.0,
+                          S=4096, rope_cols=8192),
+    "swiglu_up_4096": dict(kind="swiglu", M=4096, K=4096, F=14336),
+    "rmsnorm_chain_8192": dict(kind="rms_chain", M=8192, K=8192, d=8192, N2=8192, eps=1e-6,
+                               bwd_K=8192),
+    "lm_head_ce_8192": dict(kind="ce", M=8192, K=4096, V=32768),
+}
