@@ -1,0 +1,380 @@
+"""GB300 (sm_103a) CODA GEMM-epilogue library: Python binding.
+
+Thin marshalling over the C ABI in include/coda.h (libcoda.so, loaded with
+ctypes). Every computation runs in libcoda's CUDA kernels; this module only
+checks tensor dtypes/devices/shapes, allocates outputs with torch, passes
+pointers and the current CUDA stream, and turns error codes into exceptions.
+Function names are the C names.
+
+bf16 tensors are ``torch.bfloat16``; statistics ``torch.float32``; labels
+``torch.int32``. All tensors live on the current CUDA device.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "CodaError", "lib", "coda_init", "coda_device_status", "coda_set_wait_timeout_ns",
+    "coda_num_col_tiles", "coda_num_row_tiles", "coda_gemm", "coda_gemm_res_rmsprep", "coda_rms_reduce",
+    "coda_gemm_rowscale", "coda_gemm_swiglu", "coda_gemm_swiglu_bwd", "coda_rope_tables", "coda_gemm_rope",
+    "coda_gemm_rope_bwd", "coda_gemm_ce_lse", "coda_ce_reduce", "coda_gemm_ce_bwd", "coda_gemm_rowdot",
+    "coda_rowdot_reduce", "coda_gemm_rmsnorm_bwd", "coda_colsum_reduce", "coda_unfused_add",
+    "coda_unfused_rmsnorm", "coda_unfused_rowscale", "coda_unfused_swiglu", "coda_unfused_swiglu_bwd",
+    "coda_unfused_rope", "coda_unfused_rope_bwd", "coda_unfused_ce_fwd", "coda_unfused_ce_bwd",
+    "coda_unfused_rowdot", "coda_unfused_rmsnorm_bwd",
+]
+
+
+class CodaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libcoda error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    return _lib.load()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise CodaError(rc, lib().coda_last_error().decode(errors="replace"))
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _bf16(t, name, ndim=None):
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor (got {t.dtype} on {t.device})")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _f32(t, name):
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
+    return t
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+    return t
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ----------------------------------------------------------------- runtime
+
+def coda_init(device: int = 0):
+    _check(lib().coda_init(device))
+
+
+def coda_device_status(clear: bool = True) -> int:
+    rc = lib().coda_device_status(1 if clear else 0)
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def coda_set_wait_timeout_ns(ns: int):
+    _check(lib().coda_set_wait_timeout_ns(int(ns)))
+
+
+def coda_num_col_tiles(N: int) -> int:
+    return lib().coda_num_col_tiles(N)
+
+
+def coda_num_row_tiles(M: int) -> int:
+    return lib().coda_num_row_tiles(M)
+
+
+# ----------------------------------------------------------------- GEMMs
+
+def coda_gemm(A, B, transA: bool = False, transB: bool = False, out=None, stream=None):
+    """C = op(A) op(B). A is [M,K] (or [K,M] with transA), B is [K,N] (or [N,K])."""
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if A.dim() != 2 or B.dim() != 2 or A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B must be 2-D with unit column stride")
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if out is None:
+        out = _empty((M, N), torch.bfloat16, A)
+    if out.stride(1) != 1:
+        raise ValueError("out must have unit column stride")
+    _check(lib().coda_gemm(M, N, K, _ptr(A), A.stride(0), int(transA), _ptr(B), B.stride(0), int(transB),
+                           _ptr(out), out.stride(0), _stream(stream)))
+    return out
+
+
+def coda_gemm_res_rmsprep(x, W0, z, gamma, h1=None, h2=None, psq=None, stream=None):
+    """h1 = x W0 + z, h2 = h1 * gamma, psq = per-column-tile sums of h1^2."""
+    _bf16(x, "x", 2), _bf16(W0, "W0", 2), _bf16(z, "z", 2), _bf16(gamma, "gamma", 1)
+    M, K = x.shape
+    N = W0.shape[1]
+    if W0.shape[0] != K or z.shape != (M, N) or gamma.shape[0] != N:
+        raise ValueError("shape mismatch")
+    h1 = _empty((M, N), torch.bfloat16, x) if h1 is None else h1
+    h2 = _empty((M, N), torch.bfloat16, x) if h2 is None else h2
+    psq = _empty((M, coda_num_col_tiles(N)), torch.float32, x) if psq is None else psq
+    _check(lib().coda_gemm_res_rmsprep(M, N, K, _ptr(x), _ptr(W0), _ptr(z), _ptr(gamma), _ptr(h1), _ptr(h2),
+                                       _ptr(psq), _stream(stream)))
+    return h1, h2, psq
+
+
+def coda_rms_reduce(psq, d: int, eps: float, r=None, stream=None):
+    _f32(psq, "psq")
+    M, nb = psq.shape
+    r = _empty((M,), torch.float32, psq) if r is None else r
+    _check(lib().coda_rms_reduce(M, nb, d, _ptr(psq), float(eps), _ptr(r), _stream(stream)))
+    return r
+
+
+def coda_gemm_rowscale(h2, W1, r, out=None, stream=None):
+    _bf16(h2, "h2", 2), _bf16(W1, "W1", 2), _f32(r, "r")
+    M, K = h2.shape
+    N = W1.shape[1]
+    if W1.shape[0] != K or r.shape[0] != M:
+        raise ValueError("shape mismatch")
+    out = _empty((M, N), torch.bfloat16, h2) if out is None else out
+    _check(lib().coda_gemm_rowscale(M, N, K, _ptr(h2), _ptr(W1), _ptr(r), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_swiglu(X, Wgu, want_gu: bool = False, out=None, gu=None, stream=None):
+    """A = silu(G) * U with gate/up interleaved in the columns of X Wgu."""
+    _bf16(X, "X", 2), _bf16(Wgu, "Wgu", 2)
+    M, K = X.shape
+    F2 = Wgu.shape[1]
+    if Wgu.shape[0] != K or F2 % 2:
+        raise ValueError("shape mismatch")
+    F = F2 // 2
+    out = _empty((M, F), torch.bfloat16, X) if out is None else out
+    if want_gu and gu is None:
+        gu = _empty((M, F2), torch.bfloat16, X)
+    _check(lib().coda_gemm_swiglu(M, F, K, _ptr(X), _ptr(Wgu), _ptr(out), _ptr(gu), _stream(stream)))
+    return out, gu
+
+
+def coda_gemm_swiglu_bwd(dY, Wd, gu, out=None, stream=None):
+    """dGU (interleaved dG, dU) from dA = dY Wd^T; Wd stored [F, K]."""
+    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2), _bf16(gu, "gu", 2)
+    M, K = dY.shape
+    F = Wd.shape[0]
+    if Wd.shape[1] != K or gu.shape != (M, 2 * F):
+        raise ValueError("shape mismatch")
+    out = _empty((M, 2 * F), torch.bfloat16, dY) if out is None else out
+    _check(lib().coda_gemm_swiglu_bwd(M, F, K, _ptr(dY), _ptr(Wd), _ptr(gu), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_rope_tables(S: int, head_dim: int, theta: float, device=None, stream=None):
+    device = torch.device("cuda") if device is None else device
+    c = torch.empty((S, head_dim // 2), dtype=torch.float32, device=device)
+    s = torch.empty_like(c)
+    _check(lib().coda_rope_tables(S, head_dim, float(theta), _ptr(c), _ptr(s), _stream(stream)))
+    return c, s
+
+
+def _rope(fname, X, W, cos, sin, head_dim, rope_cols, out, stream):
+    _bf16(X, "X", 2), _bf16(W, "W", 2), _f32(cos, "cos"), _f32(sin, "sin")
+    M, K = X.shape
+    N = W.shape[1]
+    if W.shape[0] != K or cos.shape != sin.shape or cos.shape[1] != head_dim // 2:
+        raise ValueError("shape mismatch")
+    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    _check(getattr(lib(), fname)(M, N, K, _ptr(X), _ptr(W), _ptr(cos), _ptr(sin), cos.shape[0], head_dim,
+                                 rope_cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_rope(X, W, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
+    return _rope("coda_gemm_rope", X, W, cos, sin, head_dim, rope_cols, out, stream)
+
+
+def coda_gemm_rope_bwd(A, B, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
+    return _rope("coda_gemm_rope_bwd", A, B, cos, sin, head_dim, rope_cols, out, stream)
+
+
+def coda_gemm_ce_lse(H, W, labels, with_argmax: bool = True, stream=None):
+    """Per-(row, column tile) (max, sum exp, argmax) of the logits H W and the
+    target logit per row. Returns (pmax, psum, parg or None, tgt)."""
+    _bf16(H, "H", 2), _bf16(W, "W", 2), _i32(labels, "labels")
+    M, K = H.shape
+    V = W.shape[1]
+    if W.shape[0] != K or labels.shape[0] != M:
+        raise ValueError("shape mismatch")
+    nb = coda_num_col_tiles(V)
+    pmax = _empty((M, nb), torch.float32, H)
+    psum = _empty((M, nb), torch.float32, H)
+    parg = _empty((M, nb), torch.int32, H) if with_argmax else None
+    tgt = _empty((M,), torch.float32, H)
+    _check(lib().coda_gemm_ce_lse(M, V, K, _ptr(H), _ptr(W), _ptr(labels), _ptr(pmax), _ptr(psum), _ptr(parg),
+                                  _ptr(tgt), _stream(stream)))
+    return pmax, psum, parg, tgt
+
+
+def coda_ce_reduce(pmax, psum, parg, tgt, stream=None):
+    """Returns (lse, loss_row, loss_mean[1], argmax or None)."""
+    M, nb = pmax.shape
+    lse = _empty((M,), torch.float32, pmax)
+    loss_row = _empty((M,), torch.float32, pmax)
+    loss_mean = _empty((1,), torch.float32, pmax)
+    argmax = _empty((M,), torch.int32, pmax) if parg is not None else None
+    _check(lib().coda_ce_reduce(M, nb, _ptr(pmax), _ptr(psum), _ptr(parg), _ptr(tgt), _ptr(lse), _ptr(loss_row),
+                                _ptr(loss_mean), _ptr(argmax), _stream(stream)))
+    return lse, loss_row, loss_mean, argmax
+
+
+def coda_gemm_ce_bwd(H, W, labels, lse, grad_scale: float, out=None, stream=None):
+    _bf16(H, "H", 2), _bf16(W, "W", 2), _i32(labels, "labels"), _f32(lse, "lse")
+    M, K = H.shape
+    V = W.shape[1]
+    out = _empty((M, V), torch.bfloat16, H) if out is None else out
+    _check(lib().coda_gemm_ce_bwd(M, V, K, _ptr(H), _ptr(W), _ptr(labels), _ptr(lse), float(grad_scale),
+                                  _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_rowdot(dO, Wn, Y, r=None, want_dyr: bool = True, stream=None):
+    """dY = dO Wn, dYr = r * dY (optional), pdot tile partials of rowsum(dY * Y)."""
+    _bf16(dO, "dO", 2), _bf16(Wn, "Wn", 2), _bf16(Y, "Y", 2)
+    M, K = dO.shape
+    N = Wn.shape[1]
+    dY = _empty((M, N), torch.bfloat16, dO)
+    dYr = _empty((M, N), torch.bfloat16, dO) if want_dyr else None
+    pdot = _empty((M, coda_num_col_tiles(N)), torch.float32, dO)
+    _check(lib().coda_gemm_rowdot(M, N, K, _ptr(dO), _ptr(Wn), _ptr(Y), _ptr(r), _ptr(dY), _ptr(dYr), _ptr(pdot),
+                                  _stream(stream)))
+    return dY, dYr, pdot
+
+
+def coda_rowdot_reduce(pdot, d: int, stream=None):
+    M, nb = pdot.shape
+    s = _empty((M,), torch.float32, pdot)
+    _check(lib().coda_rowdot_reduce(M, nb, d, _ptr(pdot), _ptr(s), _stream(stream)))
+    return s
+
+
+def coda_gemm_rmsnorm_bwd(dY, W1, h1, gamma, r, s, stream=None):
+    """dh1 = r gamma G - r^2 s h1 with G = dY W1^T (W1 stored [d, K]); pdg column partials."""
+    _bf16(dY, "dY", 2), _bf16(W1, "W1", 2), _bf16(h1, "h1", 2), _bf16(gamma, "gamma", 1)
+    _f32(r, "r"), _f32(s, "s")
+    M, K = dY.shape
+    d = W1.shape[0]
+    dh1 = _empty((M, d), torch.bfloat16, dY)
+    pdg = _empty((coda_num_row_tiles(M), d), torch.float32, dY)
+    _check(lib().coda_gemm_rmsnorm_bwd(M, d, K, _ptr(dY), _ptr(W1), _ptr(h1), _ptr(gamma), _ptr(r), _ptr(s),
+                                       _ptr(dh1), _ptr(pdg), _stream(stream)))
+    return dh1, pdg
+
+
+def coda_colsum_reduce(pdg, stream=None):
+    rows, d = pdg.shape
+    out = _empty((d,), torch.float32, pdg)
+    _check(lib().coda_colsum_reduce(rows, d, _ptr(pdg), _ptr(out), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- unfused path
+
+def coda_unfused_add(a, b, out=None, stream=None):
+    M, N = a.shape
+    out = torch.empty_like(a) if out is None else out
+    _check(lib().coda_unfused_add(M, N, _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_unfused_rmsnorm(h, gamma, eps: float, stream=None):
+    M, d = h.shape
+    n = torch.empty_like(h)
+    r = _empty((M,), torch.float32, h)
+    _check(lib().coda_unfused_rmsnorm(M, d, _ptr(h), _ptr(gamma), float(eps), _ptr(n), _ptr(r), _stream(stream)))
+    return n, r
+
+
+def coda_unfused_rowscale(x, r, stream=None):
+    M, N = x.shape
+    out = torch.empty_like(x)
+    _check(lib().coda_unfused_rowscale(M, N, _ptr(x), _ptr(r), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_unfused_swiglu(gu, stream=None):
+    M, F2 = gu.shape
+    out = _empty((M, F2 // 2), torch.bfloat16, gu)
+    _check(lib().coda_unfused_swiglu(M, F2 // 2, _ptr(gu), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_unfused_swiglu_bwd(dA, gu, stream=None):
+    M, F = dA.shape
+    out = _empty((M, 2 * F), torch.bfloat16, dA)
+    _check(lib().coda_unfused_swiglu_bwd(M, F, _ptr(dA), _ptr(gu), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_unfused_rope(x, cos, sin, head_dim: int, rope_cols: int, stream=None):
+    """In place on x [M, N]."""
+    M, N = x.shape
+    _check(lib().coda_unfused_rope(M, N, _ptr(cos), _ptr(sin), cos.shape[0], head_dim, rope_cols, _ptr(x),
+                                   _stream(stream)))
+    return x
+
+
+def coda_unfused_rope_bwd(x, cos, sin, head_dim: int, rope_cols: int, stream=None):
+    M, N = x.shape
+    _check(lib().coda_unfused_rope_bwd(M, N, _ptr(cos), _ptr(sin), cos.shape[0], head_dim, rope_cols, _ptr(x),
+                                       _stream(stream)))
+    return x
+
+
+def coda_unfused_ce_fwd(logits, labels, stream=None):
+    M, V = logits.shape
+    lse = _empty((M,), torch.float32, logits)
+    loss_row = _empty((M,), torch.float32, logits)
+    loss_mean = _empty((1,), torch.float32, logits)
+    argmax = _empty((M,), torch.int32, logits)
+    _check(lib().coda_unfused_ce_fwd(M, V, _ptr(logits), _ptr(labels), _ptr(lse), _ptr(loss_row), _ptr(loss_mean),
+                                     _ptr(argmax), _stream(stream)))
+    return lse, loss_row, loss_mean, argmax
+
+
+def coda_unfused_ce_bwd(logits, labels, lse, grad_scale: float, stream=None):
+    M, V = logits.shape
+    out = torch.empty_like(logits)
+    _check(lib().coda_unfused_ce_bwd(M, V, _ptr(logits), _ptr(labels), _ptr(lse), float(grad_scale), _ptr(out),
+                                     _stream(stream)))
+    return out
+
+
+def coda_unfused_rowdot(dY, Y, d: int, stream=None):
+    M, N = dY.shape
+    s = _empty((M,), torch.float32, dY)
+    _check(lib().coda_unfused_rowdot(M, N, d, _ptr(dY), _ptr(Y), _ptr(s), _stream(stream)))
+    return s
+
+
+def coda_unfused_rmsnorm_bwd(G, h, gamma, r, stream=None):
+    M, d = G.shape
+    dh = torch.empty_like(G)
+    pdg = _empty((coda_num_row_tiles(M), d), torch.float32, G)
+    _check(lib().coda_unfused_rmsnorm_bwd(M, d, _ptr(G), _ptr(h), _ptr(gamma), _ptr(r), _ptr(dh), _ptr(pdg),
+                                          _stream(stream)))
+    return dh, pdg

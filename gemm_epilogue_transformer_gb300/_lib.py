@@ -1,0 +1,70 @@
+"""ctypes loader for libcoda.so with the argument types of every entry point
+declared in include/coda.h. Loading fails loudly if the library is missing:
+there is no fallback implementation."""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_double, c_float, c_int, c_uint64, c_void_p, c_char_p
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
+
+P = c_void_p  # any device pointer (bf16 / fp32 / int32) or stream handle
+I = c_int
+
+# name -> (restype, argtypes); mirrors include/coda.h
+SIGNATURES = {
+    "coda_last_error": (c_char_p, []),
+    "coda_init": (I, [I]),
+    "coda_device_status": (I, [I]),
+    "coda_set_wait_timeout_ns": (I, [c_uint64]),
+    "coda_num_col_tiles": (I, [I]),
+    "coda_num_row_tiles": (I, [I]),
+    "coda_gemm": (I, [I, I, I, P, I, I, P, I, I, P, I, P]),
+    "coda_gemm_res_rmsprep": (I, [I, I, I, P, P, P, P, P, P, P, P]),
+    "coda_rms_reduce": (I, [I, I, I, P, c_float, P, P]),
+    "coda_gemm_rowscale": (I, [I, I, I, P, P, P, P, P]),
+    "coda_gemm_swiglu": (I, [I, I, I, P, P, P, P, P]),
+    "coda_gemm_swiglu_bwd": (I, [I, I, I, P, P, P, P, P]),
+    "coda_rope_tables": (I, [I, I, c_double, P, P, P]),
+    "coda_gemm_rope": (I, [I, I, I, P, P, P, P, I, I, I, P, P]),
+    "coda_gemm_rope_bwd": (I, [I, I, I, P, P, P, P, I, I, I, P, P]),
+    "coda_gemm_ce_lse": (I, [I, I, I, P, P, P, P, P, P, P, P]),
+    "coda_ce_reduce": (I, [I, I, P, P, P, P, P, P, P, P, P]),
+    "coda_gemm_ce_bwd": (I, [I, I, I, P, P, P, P, c_float, P, P]),
+    "coda_gemm_rowdot": (I, [I, I, I, P, P, P, P, P, P, P, P]),
+    "coda_rowdot_reduce": (I, [I, I, I, P, P, P]),
+    "coda_gemm_rmsnorm_bwd": (I, [I, I, I, P, P, P, P, P, P, P, P, P]),
+    "coda_colsum_reduce": (I, [I, I, P, P, P]),
+    "coda_unfused_add": (I, [I, I, P, P, P, P]),
+    "coda_unfused_rmsnorm": (I, [I, I, P, P, c_float, P, P, P]),
+    "coda_unfused_rowscale": (I, [I, I, P, P, P, P]),
+    "coda_unfused_swiglu": (I, [I, I, P, P, P]),
+    "coda_unfused_swiglu_bwd": (I, [I, I, P, P, P, P]),
+    "coda_unfused_rope": (I, [I, I, P, P, I, I, I, P, P]),
+    "coda_unfused_rope_bwd": (I, [I, I, P, P, I, I, I, P, P]),
+    "coda_unfused_ce_fwd": (I, [I, I, P, P, P, P, P, P, P]),
+    "coda_unfused_ce_bwd": (I, [I, I, P, P, P, c_float, P, P]),
+    "coda_unfused_rowdot": (I, [I, I, I, P, P, P, P]),
+    "coda_unfused_rmsnorm_bwd": (I, [I, I, P, P, P, P, P, P, P]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libcoda.so (once) and set every entry point's signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libcoda.so not found at {path}: build it with "
+            "`python -m gemm_epilogue_transformer_gb300.build_lib` (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib

@@ -1,0 +1,457 @@
+// Epilogue programs: what runs on a 128 x 256 fp32 accumulator tile after the
+// mainloop and before the global store (CODA note, Key design 4: element/pair
+// maps, rank-1 loads, rank-2 tile loads/stores, tile partial reductions,
+// stateful transforms).
+//
+// Thread layout inside an epilogue warp: lane = one accumulator row, a chunk =
+// 32 consecutive columns of that row in registers (acc[32]). Pairs (2i, 2i+1)
+// therefore always sit in the same thread, and per-row partial reductions are
+// thread-local; per-column partials use a warp transpose-reduce.
+#pragma once
+
+#include "gemm_core.cuh"
+
+namespace coda {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float exp_f(float x) { return exp2f(x * kLog2e); }
+__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + exp_f(-g)); }
+
+// Sum each of the 32 columns held by the warp's 32 rows; afterwards lane j
+// holds the total of column j in v[0]. 31 shuffles per thread.
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// Default store coordinates: one full 32-column box per chunk per slot.
+#define CODA_STORE_SAME_COLS(MAP1)                                                                           \
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) { \
+    map = (s == 0) ? 0 : (MAP1);                                                                             \
+    x = cx.n0 + 32 * c;                                                                                      \
+    y = cx.wrow0;                                                                                            \
+  }
+
+// ------------------------------------------------------------------ identity
+struct EpiPlain {
+  struct Params {
+    int unused;
+  };
+  struct State {};
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
+  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], uint32_t box0,
+                               uint32_t) {
+    stage_row32(box0, cx.lane, acc);
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ------------------------------------------- residual + gamma + sum of squares
+// h1 = acc + z; psq += h1^2 (fp32 h1, unscaled); h2 = h1 * gamma.
+// (CODA note, Key design 1; the partial is measured on the unscaled output.)
+struct EpiResRmsPrep {
+  struct Params {
+    const __nv_bfloat16* z;
+    const __nv_bfloat16* gamma;
+    float* psq;
+  };
+  struct State {
+    float sumsq;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 2; }
+  __device__ static void begin(State& st, const Params&, const EpiCtx&) { st.sumsq = 0.f; }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
+                               uint32_t box0, uint32_t box1) {
+    const int col0 = cx.n0 + 32 * c;
+    float v[32];
+    load_row32(ep.z, cx.N, cx.M, cx.N, cx.row, col0, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      acc[i] += v[i];
+      st.sumsq = fmaf(acc[i], acc[i], st.sumsq);
+    }
+    stage_row32(box0, cx.lane, acc);
+    load_vec32(ep.gamma, cx.N, col0, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] *= v[i];
+    stage_row32(box1, cx.lane, acc);
+  }
+  CODA_STORE_SAME_COLS(1)
+  __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) ep.psq[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.sumsq;
+  }
+};
+
+// ------------------------------------------------------- delayed row scale
+// Y[i,j] = r[i] * acc[i,j] (CODA note, Key design 1).
+struct EpiRowScale {
+  struct Params {
+    const float* r;
+  };
+  struct State {
+    float rv;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], uint32_t box0,
+                               uint32_t) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] *= st.rv;
+    stage_row32(box0, cx.lane, acc);
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ---------------------------------------------------------------- SwiGLU fwd
+// Even column = gate G, odd = up U; out[f] = silu(G) * U; the 32 accumulator
+// columns of a chunk give 16 outputs, two chunks fill one 32-column store box
+// (CODA note, Key design 2: halve the width and compact before the store).
+// Optional side output: the pre-activation GU itself (bf16), for the backward.
+struct EpiSwiGLU {
+  struct Params {
+    __nv_bfloat16* gu;  // nullable, [M, 2F]
+  };
+  struct State {};
+  static constexpr int kChunksPerStore = 2;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
+  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t box0,
+                               uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    if (ep.gu != nullptr && cx.row < cx.M) {
+      uint4* dst = reinterpret_cast<uint4*>(ep.gu + static_cast<long>(cx.row) * cx.N + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (col0 + 8 * q < cx.N)
+          dst[q] = make_uint4(pack_bf16(acc[8 * q + 0], acc[8 * q + 1]), pack_bf16(acc[8 * q + 2], acc[8 * q + 3]),
+                              pack_bf16(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16(acc[8 * q + 6], acc[8 * q + 7]));
+    }
+    float o[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float g = acc[2 * k], u = acc[2 * k + 1];
+      o[k] = g * sigmoid_f(g) * u;
+    }
+    const int h = 2 * (c & 1);
+    stage_put(box0, cx.lane, h + 0, pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+              pack_bf16(o[6], o[7]));
+    stage_put(box0, cx.lane, h + 1, pack_bf16(o[8], o[9]), pack_bf16(o[10], o[11]), pack_bf16(o[12], o[13]),
+              pack_bf16(o[14], o[15]));
+  }
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
+    map = 0;
+    x = cx.n0 / 2 + 16 * (c - 1);
+    y = cx.wrow0;
+  }
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ---------------------------------------------------------------- SwiGLU bwd
+// acc = dA[:, f0..f0+31]; loads the saved GU pairs, recomputes sigmoid(G), and
+// emits interleaved (dG, dU) for 64 output columns: two store boxes.
+// (pith page, Figure 7: one incoming gradient -> both paired input gradients.)
+struct EpiSwiGLUBwd {
+  struct Params {
+    const __nv_bfloat16* gu;  // [M, 2F]
+  };
+  struct State {};
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 2; }
+  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
+  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t box0,
+                               uint32_t box1) {
+    const int f0 = cx.n0 + 32 * c;
+    const int ld = 2 * cx.N;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float g[32];
+      load_row32(ep.gu, ld, cx.M, ld, cx.row, 2 * f0 + 32 * half, g);
+      float o[32];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float G = g[2 * k], U = g[2 * k + 1], dA = acc[16 * half + k];
+        const float s = sigmoid_f(G);
+        o[2 * k] = dA * U * s * (1.0f + G * (1.0f - s));
+        o[2 * k + 1] = dA * G * s;
+      }
+      stage_row32(half ? box1 : box0, cx.lane, o);
+    }
+  }
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
+    map = 0;
+    x = 2 * (cx.n0 + 32 * c) + 32 * s;
+    y = cx.wrow0;
+  }
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ---------------------------------------------------------------- RoPE
+// Adjacent pairs (2i, 2i+1) within each head of the first rope_cols columns,
+// position = row mod S, cos/sin from the caller's fp32 tables [S, head_dim/2].
+// kSign = +1: forward rotation; -1: transposed rotation (backward).
+template <int kSign>
+struct EpiRope {
+  struct Params {
+    const float* cos_tab;
+    const float* sin_tab;
+    int S, head_dim, rope_cols;
+  };
+  struct State {
+    int pos;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.pos = (cx.row < cx.M) ? (cx.row % ep.S) : 0;
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
+                               uint32_t box0, uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    if (col0 < ep.rope_cols) {
+      const int half = ep.head_dim >> 1;
+      const int i0 = (col0 % ep.head_dim) >> 1;
+      const float* cp = ep.cos_tab + static_cast<long>(st.pos) * half + i0;
+      const float* sp = ep.sin_tab + static_cast<long>(st.pos) * half + i0;
+      float cs[16], sn[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 a = ldg_nc_v4(cp + 4 * q);
+        const uint4 b = ldg_nc_v4(sp + 4 * q);
+        cs[4 * q + 0] = __uint_as_float(a.x);
+        cs[4 * q + 1] = __uint_as_float(a.y);
+        cs[4 * q + 2] = __uint_as_float(a.z);
+        cs[4 * q + 3] = __uint_as_float(a.w);
+        sn[4 * q + 0] = __uint_as_float(b.x);
+        sn[4 * q + 1] = __uint_as_float(b.y);
+        sn[4 * q + 2] = __uint_as_float(b.z);
+        sn[4 * q + 3] = __uint_as_float(b.w);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float e = acc[2 * k], o = acc[2 * k + 1];
+        const float s = kSign > 0 ? sn[k] : -sn[k];
+        acc[2 * k] = e * cs[k] - o * s;
+        acc[2 * k + 1] = e * s + o * cs[k];
+      }
+    }
+    stage_row32(box0, cx.lane, acc);
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ---------------------------------------------------- cross-entropy forward
+// Stateful online softmax over the tile's columns (CODA note, Key design 4):
+// running max m and sum s of exp(l - m) per row, the tile argmax, and the
+// target logit when the label falls in this tile. No tile is stored.
+struct EpiCeLse {
+  struct Params {
+    const int32_t* labels;
+    float* pmax;
+    float* psum;
+    int32_t* parg;  // nullable
+    float* tgt;
+    int* status;
+  };
+  struct State {
+    float m, s;
+    int best;
+    int label;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 0; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.m = -INFINITY;
+    st.s = 0.f;
+    st.best = -1;
+    st.label = -1;
+    if (cx.row < cx.M) {
+      st.label = ep.labels[cx.row];
+      if (cx.n_blk == 0 && (st.label < 0 || st.label >= cx.N)) {
+        atomicOr(ep.status, CODA_DEVST_BAD_LABEL);
+        ep.tgt[cx.row] = __uint_as_float(0x7fc00000u);
+      }
+    }
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t,
+                               uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    float cm = -INFINITY;
+    int ci = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j >= cx.N) acc[j] = -INFINITY;
+      if (acc[j] > cm) {
+        cm = acc[j];
+        ci = j;
+      }
+    }
+    if (cm > st.m) st.best = col0 + ci;
+    const float nm = fmaxf(st.m, cm);
+    if (nm != -INFINITY) {
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sum += exp_f(acc[j] - nm);
+      st.s = st.s * exp_f(st.m - nm) + sum;
+      st.m = nm;
+    }
+    const int rel = st.label - col0;
+    if (rel >= 0 && rel < 32 && cx.row < cx.M) {
+      float t = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j == rel) t = acc[j];
+      ep.tgt[cx.row] = t;
+    }
+  }
+  __device__ static void store_coord(const Params&, const EpiCtx&, int, int, int& map, int& x, int& y) {
+    map = 0;
+    x = 0;
+    y = 0;
+  }
+  __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) {
+      const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+      ep.pmax[i] = st.m;
+      ep.psum[i] = st.s;
+      if (ep.parg) ep.parg[i] = st.best;
+    }
+  }
+};
+
+// --------------------------------------------------- cross-entropy backward
+// dl = grad_scale * (exp(l - lse_row) - [j == label]) on the recomputed logits.
+struct EpiCeBwd {
+  struct Params {
+    const int32_t* labels;
+    const float* lse;
+    float grad_scale;
+  };
+  struct State {
+    int label;
+    float lse;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.label = (cx.row < cx.M) ? ep.labels[cx.row] : -1;
+    st.lse = (cx.row < cx.M) ? ep.lse[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
+                               uint32_t box0, uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float pj = exp_f(acc[j] - st.lse);
+      if (col0 + j == st.label) pj -= 1.0f;
+      acc[j] = ep.grad_scale * pj;
+    }
+    stage_row32(box0, cx.lane, acc);
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ------------------------------------------ row statistic for RMSNorm backward
+// In the GEMM that produces dY (CODA note, Key design 3): store dY, optionally
+// dYr = r * dY, and the tile partial of sum_j dY[i,j] * Y[i,j].
+struct EpiRowdot {
+  struct Params {
+    const __nv_bfloat16* Y;
+    const float* r;  // nullable when dyr is not stored
+    float* pdot;
+    int store_dyr;
+  };
+  struct State {
+    float dot, rv;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params& ep) { return ep.store_dyr ? 2 : 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.dot = 0.f;
+    st.rv = (ep.store_dyr && cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
+                               uint32_t box0, uint32_t box1) {
+    float y[32];
+    load_row32(ep.Y, cx.N, cx.M, cx.N, cx.row, cx.n0 + 32 * c, y);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st.dot = fmaf(acc[i], y[i], st.dot);
+    stage_row32(box0, cx.lane, acc);
+    if (ep.store_dyr) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] *= st.rv;
+      stage_row32(box1, cx.lane, acc);
+    }
+  }
+  CODA_STORE_SAME_COLS(1)
+  __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot;
+  }
+};
+
+// ------------------------------------------------------ RMSNorm backward
+// acc = G = dY W1^T. dh1 = r gamma G - r^2 s h1; column partial of r G h1 over
+// the warp's 32 rows (the dgamma reduction's first level).
+struct EpiRmsNormBwd {
+  struct Params {
+    const __nv_bfloat16* h1;
+    const __nv_bfloat16* gamma;
+    const float* r;
+    const float* s;
+    float* pdg;  // [ceil(M/32), d]
+  };
+  struct State {
+    float rv, r2s;
+  };
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) {
+      st.rv = ep.r[cx.row];
+      st.r2s = st.rv * st.rv * ep.s[cx.row];
+    } else {
+      st.rv = 0.f;
+      st.r2s = 0.f;
+    }
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
+                               uint32_t box0, uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    float h[32], g[32], part[32];
+    load_row32(ep.h1, cx.N, cx.M, cx.N, cx.row, col0, h);
+    load_vec32(ep.gamma, cx.N, col0, g);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      part[i] = st.rv * acc[i] * h[i];
+      acc[i] = st.rv * g[i] * acc[i] - st.r2s * h[i];
+    }
+    stage_row32(box0, cx.lane, acc);
+    const float tot = warp_colsum32(part, cx.lane);
+    // rows past M contribute zeros; a warp slice that starts past M has no partial row
+    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
+      ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+}  // namespace coda

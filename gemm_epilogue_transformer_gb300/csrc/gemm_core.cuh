@@ -1,0 +1,383 @@
+// Persistent, warp-specialised BF16 GEMM for sm_103a with a pluggable epilogue.
+//
+// This is the "fixed GEMM mainloop" tier of CODA (CODA note, overall framework:
+// a fixed tensor-core mainloop produces accumulator tiles; a programmable
+// epilogue transforms each tile on chip before the global store; light
+// auxiliary kernels combine tile partial statistics). The mainloop is written
+// for GB300 rather than translated from the pages' Hopper design:
+//
+//   warp 0 (one thread)  TMA producer: 128B-swizzled A/B tiles into a
+//                        kStages-deep shared-memory ring (mbarrier full/empty).
+//   warp 1 (one thread)  MMA issuer: tcgen05.mma M=128 N=256 K=16, fp32
+//                        accumulators in TMEM, two accumulator buffers so the
+//                        epilogue of tile t overlaps the mainloop of tile t+1.
+//   warps 2-5            epilogue: tcgen05.ld 32 lanes x 32 columns (thread =
+//                        accumulator row), the epilogue program in registers,
+//                        bf16 results staged in 64B-swizzled shared memory and
+//                        written by TMA stores; per-row / per-column partial
+//                        statistics written directly.
+//
+// Operands: C[M,N] = op(A)[M,K] * op(B)[K,N]. A is K-major ([M,K] row-major)
+// or M-major ([K,M] row-major); B is N-major ([K,N] row-major, the weight
+// layout) or K-major ([N,K] row-major). Ragged M, N, K are handled by TMA
+// zero fill on loads and clipping on stores.
+//
+// Every mbarrier wait is bounded by %globaltimer. On expiry the kernel sets a
+// bit in the device status word, raises a CTA-wide abort flag so that the
+// other roles stop waiting, drains its own TMA loads and MMAs, frees TMEM and
+// returns. No trap, no unbounded spin.
+#pragma once
+
+#include "ptx.cuh"
+#include "../../include/coda.h"
+
+namespace coda {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kStageBoxBytes = 32 * 64;  // one epilogue TMA store box: 32 rows x 64 bytes
+constexpr int kEpiSlots = 2;             // store boxes per staging buffer
+constexpr int kEpiBufs = 2;              // staging double buffer
+constexpr int kEpiWarpBytes = kStageBoxBytes * kEpiSlots * kEpiBufs;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct GemmShape {
+  int M, N, K;
+  int a_mn, b_mn;
+  int m_blocks, n_blocks, k_blocks, num_tiles, group_m;
+  int* status;                    // device status word (CODA_DEVST_* bits)
+  unsigned long long timeout_ns;  // bound on every mbarrier wait
+};
+
+struct EpiCtx {
+  int M, N;
+  int m0, n0, m_blk, n_blk, n_blocks;
+  int row;    // this thread's accumulator row (global index)
+  int wrow0;  // first row of this warp's 32-row slice (global index)
+  int ew;     // warp quarter (TMEM lanes 32*ew .. 32*ew+31)
+  int lane;
+  int k_blocks;
+};
+
+// Tile order: groups of group_m row-blocks sweep all column blocks, so the
+// A rows of a group and the B columns in flight stay L2 resident.
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_blk, int& n_blk) {
+  const int per_group = p.group_m * p.n_blocks;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int first_m = g * p.group_m;
+  int gsz = p.m_blocks - first_m;
+  if (gsz > p.group_m) gsz = p.group_m;
+  m_blk = first_m + r % gsz;
+  n_blk = r / gsz;
+}
+
+// Bounded wait. Returns false (after flagging the status word and the CTA
+// abort flag) if the phase did not complete within timeout_ns, or if another
+// role of this CTA already aborted.
+static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const GemmShape& p,
+                                               volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      atomicOr(p.status, CODA_DEVST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmShape& p,
+                                             volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, p, abort_flag);
+}
+// Bounded wait used while draining after an abort: ignores the abort flag.
+static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// Write 16 bytes of row `r` (0..31), 16-byte chunk `c16` (0..3), into a
+// 32 x 64B staging box laid out with the TMA 64-byte swizzle.
+__device__ __forceinline__ void stage_put(uint32_t box, int r, int c16, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  st_shared_v4(box + r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4), a, b, c, d);
+}
+// Pack 32 fp32 values to bf16 and write them as one full 64-byte staging row.
+__device__ __forceinline__ void stage_row32(uint32_t box, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    stage_put(box, r, q, pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+              pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// Load 32 consecutive bf16 of a row-major [rows, cols] tensor starting at
+// (row, col0) as fp32; elements past the bounds read as 0. cols is a multiple
+// of 8, col0 a multiple of 32, so each 16-byte vector is all-in or all-out.
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* base, long ld, int rows, int cols, int row, int col0,
+                                           float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (row < rows && col0 + 8 * q < cols) u = ldg_nc_v4(base + static_cast<long>(row) * ld + col0 + 8 * q);
+    v[8 * q + 0] = bf16_lo(u.x);
+    v[8 * q + 1] = bf16_hi(u.x);
+    v[8 * q + 2] = bf16_lo(u.y);
+    v[8 * q + 3] = bf16_hi(u.y);
+    v[8 * q + 4] = bf16_lo(u.z);
+    v[8 * q + 5] = bf16_hi(u.z);
+    v[8 * q + 6] = bf16_lo(u.w);
+    v[8 * q + 7] = bf16_hi(u.w);
+  }
+}
+// 32 consecutive bf16 of a vector (same address for the whole warp: broadcast).
+__device__ __forceinline__ void load_vec32(const __nv_bfloat16* base, int n, int col0, float (&v)[32]) {
+  load_row32(base, 0, 1, n, 0, col0, v);
+}
+
+// ---------------------------------------------------------------------------
+// The kernel. Epi provides:
+//   struct Params; struct State;
+//   static constexpr int kChunksPerStore;          // 32-col chunks per store step
+//   __device__ static int  slots(const Params&);   // TMA store boxes per step (0..2)
+//   __device__ static void begin(State&, const Params&, const EpiCtx&);
+//   __device__ static void chunk(State&, const Params&, const EpiCtx&, int c, float (&acc)[32],
+//                                uint32_t box0, uint32_t box1);
+//   __device__ static void store_coord(const Params&, const EpiCtx&, int c, int slot, int& map, int& x, int& y);
+//   __device__ static void end(State&, const Params&, const EpiCtx&);
+// ---------------------------------------------------------------------------
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                         const GemmShape p, const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_epi = smem + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_epi + kEpiWarps * kEpiWarpBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t s_base = smem_u32(smem);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) fills[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords(t, p, m_blk, n_blk);
+        const int m0 = m_blk * BM, n0 = n_blk * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t a_dst = s_base + stage * kStageBytes;
+          const uint32_t b_dst = a_dst + kABytes;
+          const int k0 = kb * BK;
+          if (p.a_mn) {
+            tma_load_2d(a_dst, &tmA, fb, m0, k0);
+            tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, k0);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, k0, m0);
+          }
+          if (p.b_mn) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, fb, n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(b_dst, &tmB, fb, k0, n0);
+          }
+          fills[stage]++;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every load this thread issued has landed before the CTA exits.
+      for (int s = 0; s < kStages; ++s)
+        if (fills[s] > 0) wait_drain(full_bar(s), static_cast<uint32_t>((fills[s] - 1) & 1), p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+      // Operand descriptors. K-major: 128B rows, 8-row groups 1024B apart,
+      // K advances 32B (16 bf16) inside the swizzle atom. MN-major: 64-element
+      // MN chunks 8192B apart (LBO), 8-row K groups 1024B apart (SBO), K
+      // advances 16 rows = 2048B.
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
+        if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, p, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, p, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = s_base + stage * kStageBytes;
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024u);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(buf));
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      tc_commit(drain_bar);
+      wait_drain(drain_bar, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp & 3;
+    const uint32_t my_stage = smem_u32(s_epi) + ew * kEpiWarpBytes;
+    int local = 0;
+    int sbuf = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
+      if (!wait_bounded(tfull_bar(buf), tphase, p, abort_flag)) break;
+      tc_fence_after();
+      EpiCtx cx;
+      cx.M = p.M;
+      cx.N = p.N;
+      tile_coords(t, p, cx.m_blk, cx.n_blk);
+      cx.m0 = cx.m_blk * BM;
+      cx.n0 = cx.n_blk * BN;
+      cx.n_blocks = p.n_blocks;
+      cx.ew = ew;
+      cx.lane = lane;
+      cx.wrow0 = cx.m0 + 32 * ew;
+      cx.row = cx.wrow0 + lane;
+      cx.k_blocks = p.k_blocks;
+      typename Epi::State st;
+      Epi::begin(st, ep, cx);
+      const int nslots = Epi::slots(ep);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float acc[32];
+        tmem_ld32(tbase + 32 * c, acc);
+        if (p.k_blocks == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        }
+        const uint32_t box0 = my_stage + (sbuf * kEpiSlots + 0) * kStageBoxBytes;
+        const uint32_t box1 = box0 + kStageBoxBytes;
+        if (nslots > 0 && (c % Epi::kChunksPerStore) == 0) {
+          // the staging buffer about to be written was last read by the store
+          // group before the most recent one
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+        }
+        Epi::chunk(st, ep, cx, c, acc, box0, box1);
+        if (nslots > 0 && (c % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int s = 0; s < nslots; ++s) {
+              int map, x, y;
+              Epi::store_coord(ep, cx, c, s, map, x, y);
+              tma_store_2d(map ? &tmO1 : &tmO0, s == 0 ? box0 : box1, x, y);
+            }
+            bulk_commit();
+          }
+          sbuf ^= 1;
+        }
+      }
+      // accumulator buffer fully read: hand it back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      Epi::end(st, ep, cx);
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace coda

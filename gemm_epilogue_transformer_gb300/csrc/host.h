@@ -1,0 +1,47 @@
+// Host-side internals shared by the translation units of libcoda:
+// error reporting, per-device cache, tensor-map encoding, argument checks and
+// the launch template for the fused GEMM kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/coda.h"
+
+namespace coda {
+
+// ---------------------------------------------------------------- errors
+int fail(int code, const char* fmt, ...);
+int fail_cuda(cudaError_t e, const char* what);
+
+struct DeviceInfo {
+  int ok;
+  int sm_count;
+  int* status;  // device address of the status word
+};
+// Info for the current device (validated as sm_103); nullptr after fail().
+const DeviceInfo* current_device();
+unsigned long long wait_timeout_ns();
+
+// ---------------------------------------------------------------- checks
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+#define CODA_REQUIRE(cond, code, ...)        \
+  do {                                       \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+#define CODA_REQ_PTR16(p) CODA_REQUIRE((p) != nullptr && aligned16(p), CODA_ERR_INVALID, "%s: " #p " must be a non-null 16-byte aligned device pointer", fn)
+#define CODA_REQ_PTR4(p) CODA_REQUIRE((p) != nullptr && aligned4(p), CODA_ERR_INVALID, "%s: " #p " must be a non-null 4-byte aligned device pointer", fn)
+#define CODA_REQ_OPT16(p) CODA_REQUIRE((p) == nullptr || aligned16(p), CODA_ERR_INVALID, "%s: " #p " must be 16-byte aligned", fn)
+#define CODA_REQ_OPT4(p) CODA_REQUIRE((p) == nullptr || aligned4(p), CODA_ERR_INVALID, "%s: " #p " must be 4-byte aligned", fn)
+
+// ---------------------------------------------------------------- tensor maps
+// 2-D bf16 map over a row-major [outer, inner] array with row stride
+// `row_bytes`, box {box_inner, box_outer}, the given swizzle.
+int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+}  // namespace coda

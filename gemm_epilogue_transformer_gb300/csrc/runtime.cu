@@ -1,0 +1,154 @@
+// libcoda runtime: error text, per-device initialisation and the device
+// status word, wait-timeout setting, tensor-map encoding via the driver entry
+// point (no link-time dependency on libcuda).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "host.h"
+
+namespace coda {
+
+static thread_local char g_err[1024] = "";
+static unsigned long long g_timeout_ns = 2000000000ull;
+
+// The device status word (CODA_DEVST_* bits). Kernels receive its device
+// address, obtained per device with cudaGetSymbolAddress.
+__device__ int g_device_status = 0;
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(CODA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+static std::mutex g_mu;
+static DeviceInfo g_dev[64];
+
+static const DeviceInfo* init_device(int dev) {
+  if (dev < 0 || dev >= 64) {
+    fail(CODA_ERR_INVALID, "device index %d out of range", dev);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.ok) return &d;
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) {
+    fail_cuda(e, "cudaGetDeviceProperties");
+    return nullptr;
+  }
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    fail(CODA_ERR_UNSUPPORTED, "device %d is sm_%d%d (%s); libcoda is built for sm_103a (GB300)", dev, prop.major,
+         prop.minor, prop.name);
+    return nullptr;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_device_status);
+  if (e != cudaSuccess) {
+    fail_cuda(e, "cudaGetSymbolAddress(status word)");
+    return nullptr;
+  }
+  d.sm_count = prop.multiProcessorCount;
+  d.status = static_cast<int*>(p);
+  d.ok = 1;
+  return &d;
+}
+
+const DeviceInfo* current_device() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    fail_cuda(e, "cudaGetDevice");
+    return nullptr;
+  }
+  return init_device(dev);
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CODA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(CODA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): inner %llu outer %llu stride %llu box %u x %u",
+                static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
+                (unsigned long long)row_bytes, box_inner, box_outer);
+  return CODA_OK;
+}
+
+}  // namespace coda
+
+using namespace coda;
+
+extern "C" {
+
+const char* coda_last_error(void) { return g_err; }
+
+int coda_init(int device) {
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaSetDevice");
+  return init_device(device) ? CODA_OK : CODA_ERR_UNSUPPORTED;
+}
+
+int coda_device_status(int clear) {
+  const DeviceInfo* d = current_device();
+  if (!d) return CODA_ERR_UNSUPPORTED;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "read status word");
+  if (clear) {
+    int z = 0;
+    e = cudaMemcpy(d->status, &z, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "clear status word");
+  }
+  return v;
+}
+
+int coda_set_wait_timeout_ns(unsigned long long ns) {
+  if (ns < 100000ull) return fail(CODA_ERR_INVALID, "coda_set_wait_timeout_ns: %llu ns is below 1e5", ns);
+  g_timeout_ns = ns;
+  return CODA_OK;
+}
+
+int coda_num_col_tiles(int N) { return N <= 0 ? 0 : (N + 255) / 256; }
+int coda_num_row_tiles(int M) { return M <= 0 ? 0 : (M + 31) / 32; }
+
+}  // extern "C"

@@ -1,0 +1,265 @@
+/*
+ * coda.h - C ABI of libcoda: BF16 GEMMs on GB300 (sm_103a) whose output tile
+ * is transformed on chip by a small epilogue program before it is stored, plus
+ * the light auxiliary reductions that combine the epilogues' tile partials,
+ * and an unfused comparison path (plain GEMM + separate element-wise kernels).
+ *
+ * The method is CODA, "Rewriting Transformer Blocks as GEMM-Epilogue Programs".
+ * Citations name the page and the passage:
+ *   "CODA note"  the papernotes.org note on the paper (method section, Key
+ *                designs 1-4; kernel and block speedup tables);
+ *   "pith page"  the pith.science page on arXiv 2605.19269 (figure captions,
+ *                Appendix A.1).
+ *
+ * Conventions for every entry point
+ *   - Tensors are device pointers, allocated and owned by the caller. The
+ *     library never allocates, frees or retains caller memory.
+ *   - bf16 tensors are passed as coda_bf16 (uint16_t bit patterns), row-major
+ *     and contiguous unless a leading dimension (in elements) is given.
+ *     Statistics are fp32, labels int32. Weights are [K, N] row-major.
+ *   - Base pointers of bf16 tensors and vectors and of fp32 tables must be
+ *     16-byte aligned; every row stride must be a multiple of 16 bytes
+ *     (8 bf16 elements). fp32 / int32 vectors (r, s, lse, labels, partials)
+ *     need only natural alignment.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and do not synchronise. Outputs must not alias inputs
+ *     unless stated.
+ *   - A dimension of 0 makes the call a no-op that returns CODA_OK (an empty
+ *     contraction, K = 0, gives a zero accumulator and the epilogue still runs).
+ *   - Return value: CODA_OK, or a negative CODA_ERR_*; coda_last_error()
+ *     describes the last failure on the calling thread. Argument errors are
+ *     detected on the host before anything is launched.
+ *   - Kernels never trap. Each mbarrier wait inside them is bounded; a wait
+ *     that runs out sets CODA_DEVST_TIMEOUT in the device status word and the
+ *     kernel returns early. Out-of-range labels set CODA_DEVST_BAD_LABEL.
+ *     Read (and clear) the word with coda_device_status().
+ */
+#ifndef CODA_H_
+#define CODA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CODA_OK 0
+#define CODA_ERR_INVALID (-1)     /* null pointer, misalignment, bad dimension   */
+#define CODA_ERR_UNSUPPORTED (-2) /* shape granularity not supported, not sm_103 */
+#define CODA_ERR_CUDA (-3)        /* a CUDA runtime / driver call failed         */
+#define CODA_ERR_TIMEOUT (-4)     /* device status word reported a timeout       */
+
+#define CODA_DEVST_TIMEOUT 1   /* a bounded in-kernel wait ran out            */
+#define CODA_DEVST_BAD_LABEL 2 /* a cross-entropy label was outside [0, V)    */
+
+typedef uint16_t coda_bf16;
+typedef void* coda_stream_t;
+
+/* ------------------------------------------------------------------ runtime */
+
+/* Thread-local text of the last error (empty string if none). */
+const char* coda_last_error(void);
+
+/* Make `device` current, check it is compute capability 10.3 (GB300), cache its
+ * SM count. Other calls do this lazily for the current device. */
+int coda_init(int device);
+
+/* Synchronise the current device, return the device status word
+ * (CODA_DEVST_* bits, >= 0) and, if `clear` != 0, reset it to 0.
+ * Returns CODA_ERR_CUDA if the synchronisation fails. */
+int coda_device_status(int clear);
+
+/* Bound on every in-kernel mbarrier wait, in nanoseconds (default 2e9).
+ * Values below 1e5 are rejected with CODA_ERR_INVALID. */
+int coda_set_wait_timeout_ns(unsigned long long ns);
+
+/* Number of column tiles of a fused kernel's output for GEMM width N
+ * (ceil(N / 256)): the second dimension of every [M, nb] partial buffer. */
+int coda_num_col_tiles(int N);
+
+/* Number of row tiles used by the column partials of coda_gemm_rmsnorm_bwd
+ * and coda_unfused_rmsnorm_bwd (ceil(M / 32)). */
+int coda_num_row_tiles(int M);
+
+/* ---------------------------------------------------------- plain GEMM (a1)
+ * C[M,N] = op(A) op(B), bf16 in, fp32 accumulate on the tensor cores, bf16 out.
+ * The fixed mainloop of CODA (CODA note, overall framework) with the identity
+ * epilogue. transA = 0: A is [M,K] row-major (lda >= K); transA = 1: A is
+ * stored [K,M] row-major (lda >= M) and used transposed. transB = 0: B is
+ * [K,N] row-major (ldb >= N); transB = 1: B is stored [N,K] (ldb >= K).
+ * ldc >= N. N and K multiples of 8 (with transA, M as well). */
+int coda_gemm(int M, int N, int K, const coda_bf16* A, int lda, int transA, const coda_bf16* B, int ldb,
+              int transB, coda_bf16* C, int ldc, coda_stream_t stream);
+
+/* --------------------------------------------- GEMM-RMSNorm-GEMM forward (a2-a4)
+ * CODA note, Key design 1: RMSNorm(x W0 + z, gamma) W1 = r ((x W0 + z) (.) gamma) W1
+ * with r the per-row inverse RMS, applied in the second GEMM's epilogue.
+ *
+ * coda_gemm_res_rmsprep: first GEMM, epilogue h1 = x W0 + z, h2 = h1 (.) gamma,
+ *   psq[i, t] = sum over the columns of tile t of h1[i,j]^2 (fp32 h1, before
+ *   rounding; the pages' tile partial of the unscaled residual).
+ *   x [M,K], W0 [K,N], z [M,N], gamma [N] -> h1, h2 [M,N] bf16,
+ *   psq [M, coda_num_col_tiles(N)] fp32. N, K multiples of 8. */
+int coda_gemm_res_rmsprep(int M, int N, int K, const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+                          const coda_bf16* gamma, coda_bf16* h1_out, coda_bf16* h2_out, float* psq_out,
+                          coda_stream_t stream);
+
+/* Auxiliary reduction (pith page, Figures 4 and 5):
+ * r[i] = 1 / sqrt(sum_t psq[i,t] / d + eps). psq [M, nb] fp32 -> r [M] fp32. */
+int coda_rms_reduce(int M, int nb, int d, const float* psq, float eps, float* r_out, coda_stream_t stream);
+
+/* Second GEMM with the delayed row scale (CODA note, Key design 1):
+ * Y[i,j] = r[i] (h2 W1)[i,j]. h2 [M,K], W1 [K,N], r [M] -> Y [M,N] bf16. */
+int coda_gemm_rowscale(int M, int N, int K, const coda_bf16* h2, const coda_bf16* W1, const float* r,
+                       coda_bf16* Y_out, coda_stream_t stream);
+
+/* ----------------------------------------------------------- SwiGLU (a5, a6)
+ * CODA note, Key design 2; pith page, Figure 7: gate and up channels are
+ * interleaved (even column = gate G, odd = up U).
+ *
+ * coda_gemm_swiglu: GU = X Wgu; A[:, f] = silu(GU[:, 2f]) GU[:, 2f+1].
+ *   X [M,K], Wgu [K, 2F] -> A [M,F] bf16; gu_out [M,2F] bf16 (the
+ *   pre-activation saved for the backward) or NULL. F multiple of 8. */
+int coda_gemm_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* Wgu, coda_bf16* A_out,
+                     coda_bf16* gu_out, coda_stream_t stream);
+
+/* coda_gemm_swiglu_bwd: dA = dY Wd^T (Wd stored [F, K]: the down-projection
+ *   weight), epilogue recomputes sigmoid(G) from gu and emits, interleaved,
+ *   dG = dA U s (1 + G (1 - s)), dU = dA G s with s = sigmoid(G).
+ *   dY [M,K], Wd [F,K], gu [M,2F] -> dgu [M,2F] bf16. */
+int coda_gemm_swiglu_bwd(int M, int F, int K, const coda_bf16* dY, const coda_bf16* Wd, const coda_bf16* gu,
+                         coda_bf16* dgu_out, coda_stream_t stream);
+
+/* ------------------------------------------------------------- RoPE (a7, a8)
+ * CODA note, Key design 2: rotation of adjacent channel pairs (2i, 2i+1) of
+ * each head with pre-broadcast cos/sin vectors.
+ *
+ * coda_rope_tables: cos_tab[p, i] = cos(p theta^(-2i/head_dim)), sin_tab
+ *   likewise, evaluated in fp64 and rounded to fp32; [S, head_dim/2]. */
+int coda_rope_tables(int S, int head_dim, double theta, float* cos_out, float* sin_out, coda_stream_t stream);
+
+/* coda_gemm_rope: P = X W; for columns c < rope_cols (the Q and K heads) with
+ *   pair i = (c mod head_dim) / 2 at position p = row mod S:
+ *   out_e = a_e cos - a_o sin, out_o = a_e sin + a_o cos; columns at or
+ *   beyond rope_cols (V) pass through.
+ *   X [M,K], W [K,N], cos/sin [S, head_dim/2] fp32 -> out [M,N] bf16.
+ *   head_dim a multiple of 32, rope_cols a multiple of head_dim and <= N. */
+int coda_gemm_rope(int M, int N, int K, const coda_bf16* X, const coda_bf16* W, const float* cos_tab,
+                   const float* sin_tab, int S, int head_dim, int rope_cols, coda_bf16* out, coda_stream_t stream);
+
+/* coda_gemm_rope_bwd: the same GEMM with the transposed rotation in the
+ *   epilogue (duality rule, CODA note, Key design 3): g_e = a_e cos + a_o sin,
+ *   g_o = -a_e sin + a_o cos. Arguments as coda_gemm_rope. */
+int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16* B, const float* cos_tab,
+                       const float* sin_tab, int S, int head_dim, int rope_cols, coda_bf16* out,
+                       coda_stream_t stream);
+
+/* ---------------------------------------------------- cross-entropy (a9, a10)
+ * CODA note, Key design 4 (stateful online log-sum-exp across vocabulary
+ * tiles, combined by an auxiliary reduction). Logits L = H W are fp32 in the
+ * accumulator and are never stored.
+ *
+ * coda_gemm_ce_lse: per (row i, column tile t): pmax[i,t] = max_j L[i,j],
+ *   psum[i,t] = sum_j exp(L[i,j] - pmax[i,t]), parg[i,t] = lowest j attaining
+ *   the max (NULL to skip); the tile that holds label y_i writes
+ *   tgt[i] = L[i, y_i]. H [M,K], W [K,V], labels [M] int32 in [0,V) ->
+ *   pmax, psum [M, coda_num_col_tiles(V)] fp32, parg same shape int32, tgt [M].
+ *   A label outside [0, V) sets CODA_DEVST_BAD_LABEL and tgt[i] = NaN. */
+int coda_gemm_ce_lse(int M, int V, int K, const coda_bf16* H, const coda_bf16* W, const int32_t* labels,
+                     float* pmax_out, float* psum_out, int32_t* parg_out, float* tgt_out, coda_stream_t stream);
+
+/* coda_ce_reduce: LSE_i = Mx + ln sum_t psum[i,t] exp(pmax[i,t] - Mx),
+ *   Mx = max_t pmax[i,t]; loss_row_i = LSE_i - tgt_i; loss_mean = (1/M) sum_i
+ *   loss_row_i (single scalar, NULL to skip); argmax_i from parg (lowest
+ *   column among equal maxima; NULL parg or argmax_out to skip). */
+int coda_ce_reduce(int M, int nb, const float* pmax, const float* psum, const int32_t* parg, const float* tgt,
+                   float* lse_out, float* loss_row_out, float* loss_mean_out, int32_t* argmax_out,
+                   coda_stream_t stream);
+
+/* coda_gemm_ce_bwd: recomputes the logits tile and emits
+ *   dl[i,j] = grad_scale (exp(L[i,j] - lse_i) - [j == y_i]) in bf16
+ *   (grad_scale = g / M for the mean loss). H [M,K], W [K,V], labels [M],
+ *   lse [M] -> dl [M,V] bf16. dH = dl W^T and dW = H^T dl are coda_gemm calls. */
+int coda_gemm_ce_bwd(int M, int V, int K, const coda_bf16* H, const coda_bf16* W, const int32_t* labels,
+                     const float* lse, float grad_scale, coda_bf16* dl_out, coda_stream_t stream);
+
+/* ------------------------------------- GEMM-RMSNorm-GEMM backward (a11, a12)
+ * CODA note, Key design 3: s = (1/d) rowsum(dY (.) Y) is formed in the
+ * epilogue of the GEMM that produces dY.
+ *
+ * coda_gemm_rowdot: dY = dO Wn; stores dY (bf16), optionally dYr = r (.)row dY
+ *   (bf16; NULL to skip, r may then be NULL), and pdot[i,t] = sum over the
+ *   columns of tile t of dY[i,j] Y[i,j] (fp32 dY times the stored bf16 Y).
+ *   dO [M,K], Wn [K,N], Y [M,N] -> dY, dYr [M,N], pdot [M, coda_num_col_tiles(N)]. */
+int coda_gemm_rowdot(int M, int N, int K, const coda_bf16* dO, const coda_bf16* Wn, const coda_bf16* Y,
+                     const float* r, coda_bf16* dY_out, coda_bf16* dYr_out, float* pdot_out, coda_stream_t stream);
+
+/* coda_rowdot_reduce: s[i] = sum_t pdot[i,t] / d. */
+int coda_rowdot_reduce(int M, int nb, int d, const float* pdot, float* s_out, coda_stream_t stream);
+
+/* coda_gemm_rmsnorm_bwd: G = dY W1^T (W1 stored [d, K] row-major, the forward
+ *   weight of the second GEMM); epilogue dh1 = r gamma (.) G - r^2 s h1 and
+ *   column partials pdg[b, j] = sum over rows of row tile b of r_i G[i,j] h1[i,j].
+ *   dY [M,K], W1 [d,K], h1 [M,d] bf16, gamma [d] bf16, r, s [M] fp32 ->
+ *   dh1 [M,d] bf16, pdg [coda_num_row_tiles(M), d] fp32. */
+int coda_gemm_rmsnorm_bwd(int M, int d, int K, const coda_bf16* dY, const coda_bf16* W1, const coda_bf16* h1,
+                          const coda_bf16* gamma, const float* r, const float* s, coda_bf16* dh1_out,
+                          float* pdg_out, coda_stream_t stream);
+
+/* coda_colsum_reduce: dgamma[j] = sum_b pdg[b, j]. pdg [rows, d] -> [d] fp32. */
+int coda_colsum_reduce(int rows, int d, const float* pdg, float* dgamma_out, coda_stream_t stream);
+
+/* -------------------------------------------------- unfused comparison path
+ * The memory-bound operators CODA removes, as separate HBM-bound kernels that
+ * read and write every intermediate (CODA note, research background). Each
+ * reads bf16 tensors and writes bf16 tensors; statistics are fp32. */
+
+/* out = a + b, [M,N] bf16 (out may alias a or b). */
+int coda_unfused_add(int M, int N, const coda_bf16* a, const coda_bf16* b, coda_bf16* out, coda_stream_t stream);
+
+/* Textbook RMSNorm: r_i = 1/sqrt(mean_j h[i,j]^2 + eps), n = r h (.) gamma.
+ * h [M,d], gamma [d] -> n [M,d] bf16, r [M] fp32 (r_out may be NULL). */
+int coda_unfused_rmsnorm(int M, int d, const coda_bf16* h, const coda_bf16* gamma, float eps, coda_bf16* n_out,
+                         float* r_out, coda_stream_t stream);
+
+/* out = r (.)row x, [M,N] bf16. */
+int coda_unfused_rowscale(int M, int N, const coda_bf16* x, const float* r, coda_bf16* out, coda_stream_t stream);
+
+/* A = silu(gu[:, 0::2]) gu[:, 1::2]; gu [M,2F] -> A [M,F]. */
+int coda_unfused_swiglu(int M, int F, const coda_bf16* gu, coda_bf16* A_out, coda_stream_t stream);
+
+/* dgu from dA [M,F] and gu [M,2F] (formulas as coda_gemm_swiglu_bwd). */
+int coda_unfused_swiglu_bwd(int M, int F, const coda_bf16* dA, const coda_bf16* gu, coda_bf16* dgu_out,
+                            coda_stream_t stream);
+
+/* In-place RoPE (forward) / transposed rotation (backward) on x [M,N] bf16. */
+int coda_unfused_rope(int M, int N, const float* cos_tab, const float* sin_tab, int S, int head_dim, int rope_cols,
+                      coda_bf16* x, coda_stream_t stream);
+int coda_unfused_rope_bwd(int M, int N, const float* cos_tab, const float* sin_tab, int S, int head_dim,
+                          int rope_cols, coda_bf16* x, coda_stream_t stream);
+
+/* Cross-entropy over materialised bf16 logits [M,V]: lse, loss_row [M],
+ * loss_mean (scalar, NULL to skip), argmax [M] (NULL to skip). */
+int coda_unfused_ce_fwd(int M, int V, const coda_bf16* logits, const int32_t* labels, float* lse_out,
+                        float* loss_row_out, float* loss_mean_out, int32_t* argmax_out, coda_stream_t stream);
+
+/* dl = grad_scale (softmax(logits) - onehot(labels)) from bf16 logits and lse. */
+int coda_unfused_ce_bwd(int M, int V, const coda_bf16* logits, const int32_t* labels, const float* lse,
+                        float grad_scale, coda_bf16* dl_out, coda_stream_t stream);
+
+/* s_i = (1/d) sum_j dY[i,j] Y[i,j] over bf16 dY, Y [M,N]. */
+int coda_unfused_rowdot(int M, int N, int d, const coda_bf16* dY, const coda_bf16* Y, float* s_out,
+                        coda_stream_t stream);
+
+/* Textbook RMSNorm backward from G = dL/dn [M,d], h [M,d], gamma [d], r [M]:
+ * c_i = (1/d) sum_j G gamma h, dh = r gamma G - r^3 c h; column partials
+ * pdg [coda_num_row_tiles(M), d] of r G h (reduce with coda_colsum_reduce). */
+int coda_unfused_rmsnorm_bwd(int M, int d, const coda_bf16* G, const coda_bf16* h, const coda_bf16* gamma,
+                             const float* r, coda_bf16* dh_out, float* pdg_out, coda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CODA_H_ */

@@ -9,3 +9,21 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
     config.addinivalue_line("markers", "slow: full-size parity case (minutes)")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def coda():
+    """The product binding on cuda:0, built for sm_103a if needed."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemm_epilogue_transformer_gb300 import build_lib
+    build_lib.build()
+    import gemm_epilogue_transformer_gb300 as G
+    G.coda_init(0)
+    G.coda_device_status(clear=True)
+    yield G
+    assert G.coda_device_status(clear=True) == 0, "device status word set during the tests"

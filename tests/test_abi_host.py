@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point include/coda.h declares with the binding's
+signature table, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_epilogue_transformer_gb300 import build_lib, _lib
+    build_lib.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(coda_\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("coda_gemm", "coda_gemm_res_rmsprep", "coda_rms_reduce", "coda_gemm_rowscale",
+                     "coda_gemm_swiglu", "coda_gemm_rope", "coda_gemm_ce_lse", "coda_gemm_swiglu_bwd",
+                     "coda_gemm_rope_bwd", "coda_gemm_ce_bwd", "coda_gemm_rowdot", "coda_gemm_rmsnorm_bwd",
+                     "coda_unfused_add", "coda_unfused_rmsnorm"):
+        assert required in names
+    assert len(names) == len(set(names))
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    from gemm_epilogue_transformer_gb300 import _lib
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported by libcoda.so"
+        assert n in _lib.SIGNATURES, f"{n} has no binding signature"
+    assert set(_lib.SIGNATURES) == set(names)
+
+
+def test_argument_count_matches_header():
+    from gemm_epilogue_transformer_gb300 import _lib
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for m in re.finditer(r"(coda_\w+)\s*\(([^)]*)\)\s*;", src):
+        name, args = m.group(1), m.group(2).strip()
+        n = 0 if args in ("", "void") else args.count(",") + 1
+        assert len(_lib.SIGNATURES[name][1]) == n, name
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    INVALID, UNSUPPORTED = -1, -2
+    good = _p(0x10000)
+    odd = _p(0x10008)
+    # negative / inconsistent dimensions
+    assert lib.coda_gemm(-1, 8, 8, good, 8, 0, good, 8, 0, good, 8, None) == INVALID
+    assert lib.coda_gemm(8, 8, 8, good, 8, 2, good, 8, 0, good, 8, None) == INVALID
+    assert b"transA" in lib.coda_last_error()
+    # null and misaligned pointers
+    assert lib.coda_gemm(8, 8, 8, None, 8, 0, good, 8, 0, good, 8, None) == INVALID
+    assert lib.coda_gemm(8, 8, 8, odd, 8, 0, good, 8, 0, good, 8, None) == INVALID
+    assert b"16-byte" in lib.coda_last_error()
+    # leading dimensions
+    assert lib.coda_gemm(8, 16, 8, good, 4, 0, good, 16, 0, good, 16, None) == INVALID
+    assert lib.coda_gemm(8, 16, 8, good, 8, 0, good, 16, 0, good, 12, None) == INVALID
+    # granularity
+    assert lib.coda_gemm_rowscale(8, 12, 8, good, good, good, good, None) == UNSUPPORTED
+    assert lib.coda_gemm_swiglu(8, 12, 8, good, good, good, None, None) == UNSUPPORTED
+    assert lib.coda_gemm_rope(8, 256, 8, good, good, good, good, 16, 48, 128, good, None) == UNSUPPORTED
+    assert lib.coda_gemm_rope(8, 256, 8, good, good, good, good, 16, 64, 96, good, None) == INVALID
+    assert lib.coda_gemm_rope(8, 256, 8, good, good, good, good, 0, 64, 128, good, None) == INVALID
+    assert lib.coda_rms_reduce(8, 0, 8, good, 1e-6, good, None) == INVALID
+    assert lib.coda_rms_reduce(8, 2, 8, good, -1.0, good, None) == INVALID
+    assert lib.coda_set_wait_timeout_ns(10) == INVALID
+    assert lib.coda_unfused_rmsnorm_bwd(8, 65536, good, good, good, good, good, good, None) == UNSUPPORTED
+    # empty problems are no-ops that never touch the device
+    assert lib.coda_gemm(0, 8, 8, None, 8, 0, None, 8, 0, None, 8, None) == 0
+    assert lib.coda_gemm_res_rmsprep(0, 8, 8, None, None, None, None, None, None, None, None) == 0
+    assert lib.coda_gemm_ce_lse(0, 8, 8, None, None, None, None, None, None, None, None) == 0
+    assert lib.coda_unfused_add(0, 8, None, None, None, None) == 0
+
+
+def test_tile_counts(lib):
+    assert [lib.coda_num_col_tiles(n) for n in (0, 1, 256, 257, 32768)] == [0, 1, 1, 2, 128]
+    assert [lib.coda_num_row_tiles(m) for m in (0, 1, 32, 33, 8192)] == [0, 1, 1, 2, 256]
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    good = _p(0x10000)
+    rc = lib.coda_gemm(128, 256, 64, good, 64, 0, good, 256, 0, good, 256, None)
+    assert rc in (-2, -3)
+    assert lib.coda_last_error()

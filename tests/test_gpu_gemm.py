@@ -1,0 +1,64 @@
+"""Parity of the plain tcgen05 GEMM (identity epilogue) with the float64 oracle,
+all four operand layouts, shapes spanning several tiles with ragged tails."""
+import numpy as np
+import pytest
+
+import coda_inputs as gen
+import oracle as O
+from _util import assert_bf16, dev_bf16, f64
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    (128, 256, 64),     # one tile, one k-block
+    (256, 512, 512),    # 2 x 2 tiles, 8 k-blocks
+    (300, 520, 200),    # ragged M, N, K
+    (64, 8, 8),         # smaller than one tile in every dimension
+    (1, 264, 136),      # single row
+    (640, 1024, 2048),  # 5 x 4 tiles, 32 k-blocks
+    (2560, 4096, 128),  # 320 tiles: two or three tiles per persistent CTA
+    (4096, 3072, 264),  # 384 tiles, ragged K
+]
+
+
+def _operands(M, N, K, ta, tb, seed):
+    rngs = [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(2)]
+    A = gen.normal_bf16(rngs[0], (K, M) if ta else (M, K))
+    B = gen.normal_bf16(rngs[1], (N, K) if tb else (K, N), std=1.0 / np.sqrt(max(K, 1)))
+    return A, B
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_parity(coda, M, N, K, ta, tb):
+    if ta and M % 8:
+        pytest.skip("transposed A needs M % 8 == 0 (16-byte rows)")
+    A, B = _operands(M, N, K, ta, tb, seed=M * 7 + N * 3 + K + ta * 2 + tb)
+    C = coda.coda_gemm(dev_bf16(A), dev_bf16(B), transA=bool(ta), transB=bool(tb))
+    a = O.bf16(A).T if ta else O.bf16(A)
+    b = O.bf16(B).T if tb else O.bf16(B)
+    assert_bf16(f64(C), O.matmul(a, b), f"gemm {M}x{N}x{K} ta={ta} tb={tb}")
+
+
+def test_gemm_k_zero_and_empty(coda):
+    import torch
+    A = torch.zeros((16, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((0, 24), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((16, 24), 7.0, dtype=torch.bfloat16, device="cuda")
+    coda.coda_gemm(A, B, out=C)
+    assert float(C.float().abs().max()) == 0.0
+    E = coda.coda_gemm(torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda"),
+                       torch.zeros((64, 16), dtype=torch.bfloat16, device="cuda"))
+    assert E.shape == (0, 16)
+
+
+def test_gemm_leading_dims(coda):
+    """Row strides larger than the logical width (views into wider buffers)."""
+    M, N, K = 200, 136, 72
+    A, B = _operands(M, N + 24, K + 40, 0, 0, seed=5)
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    import torch
+    out = torch.zeros((M, N + 56), dtype=torch.bfloat16, device="cuda")
+    coda.coda_gemm(dA[:, :K], dB[:K, :N], out=out[:, :N])
+    assert_bf16(f64(out[:, :N]), O.matmul(O.bf16(A)[:, :K], O.bf16(B)[:K, :N]), "gemm strided")
+    assert float(out[:, N:].float().abs().max()) == 0.0, "wrote past the logical columns"
