@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark of the CODA GEMM-epilogue hot path on GB300.
+
+Workload (default): the GEMM+RoPE QKV projection, X[4096,4096] x W[4096,12288]
+bf16, RoPE on the Q and K heads (head_dim 128, theta 10000, positions
+0..4095, adjacent pairs), forward and backward. One step is
+
+  QKV = rope(X W)                      coda_gemm_rope       (fused epilogue)
+  dP  = rope^T(A B)                    coda_gemm_rope_bwd   (fused epilogue;
+                                       A B stands in for the upstream gradient)
+  dX  = dP W^T,  dW = X^T dP           coda_gemm x 2        (plain GEMMs)
+
+4 x 2 M N K = 1.649 TFLOP per step. The unfused comparison runs the same GEMMs
+with the identity epilogue plus separate in-place RoPE kernels.
+
+Prints one JSON line (rank 0). `--impl reference` times the float64 CPU oracle
+on a bounded sample of the same workload instead. Multi-GPU: replicas only
+(every rank runs the whole workload; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s (% BF16 TC peak) and speedup vs unfused path"
+WL = dict(name="rope_qkv_4096", M=4096, K=4096, N=12288, head_dim=128, theta=10000.0, S=4096, rope_cols=8192)
+FLOPS_PER_GEMM = 2.0 * WL["M"] * WL["N"] * WL["K"]
+FLOPS_PER_STEP = 4 * FLOPS_PER_GEMM
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    return ap.parse_args()
+
+
+def config():
+    return {"workload": "GEMM+RoPE QKV projection fwd+bwd: X[4096,4096] x W[4096,12288] bf16, "
+                        "RoPE on Q,K (head_dim 128, theta 1e4, positions 0..4095), dX/dW GEMMs",
+            "M": WL["M"], "K": WL["K"], "N": WL["N"], "head_dim": WL["head_dim"], "rope_cols": WL["rope_cols"],
+            "flops_per_step": FLOPS_PER_STEP, "l2": "flushed between steps (256 MiB write), inputs 256 MiB"}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(inputs, rows):
+    """The float64 oracle on the first `rows` tokens of each of the step's four
+    GEMMs; returns (seconds, flops)."""
+    import oracle as O
+    pos = np.arange(rows) % WL["S"]
+    X = O.bf16(inputs["X"][:rows])
+    A = O.bf16(inputs["A"][:rows])
+    W = inputs["_W64"]
+    B = inputs["_B64"]
+    t0 = time.perf_counter()
+    O.gemm_rope(X, W, pos, WL["head_dim"], WL["theta"], WL["rope_cols"])
+    dP = O.gemm_rope_bwd(A, B, pos, WL["head_dim"], WL["theta"], WL["rope_cols"])
+    O.matmul(dP, W.T)
+    O.matmul(X.T, dP)
+    return time.perf_counter() - t0, 4 * 2.0 * rows * WL["K"] * WL["N"]
+
+
+def oracle_prepare(inputs):
+    import oracle as O
+    inputs["_W64"] = O.bf16(inputs["W"])
+    inputs["_B64"] = O.bf16(inputs["B"])
+
+
+def calibrate_rows(inputs, target_s):
+    t, _ = oracle_sample(inputs, 32)
+    rows = int(32 * target_s / max(t, 1e-3))
+    return max(32, min(WL["M"], rows // 32 * 32))
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(inputs):
+    oracle_prepare(inputs)
+    rows = calibrate_rows(inputs, 12.0)
+    t, fl = oracle_sample(inputs, rows)
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+            "sample": f"first {rows} of 4096 token rows of each of the 4 GEMMs of one step (float64 NumPy, "
+                      f"{t:.1f} s)"}
+
+
+# ---------------------------------------------------------------- GPU helpers
+
+class Clocks:
+    """nvidia-smi sampler running during the timed regions."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait(timeout=10)
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = np.array([float(r[1]) for r in rows])
+        mx = float(rows[0][2])
+        load = sm[sm >= 0.5 * mx] if np.any(sm >= 0.5 * mx) else sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d["hbm_gbs"], "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def kernel_src_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gemm_epilogue_transformer_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("src_hash") != kernel_src_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def main():
+    a = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import coda_inputs as gen
+    if a.impl == "reference":
+        return reference_arm(a, rank, world)
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from gemm_epilogue_transformer_gb300 import build_lib
+    if rank == 0 or world == 1:
+        build_lib.build()
+    if dist:
+        dist.barrier()
+    import gemm_epilogue_transformer_gb300 as G
+    G.coda_init(local)
+
+    p = gen.rope_problem(WL["M"], WL["K"], WL["N"], seed=0)
+    dev = torch.device("cuda", local)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    host = {k: bf(v).pin_memory() for k, v in p.items()}
+    X, W, A, B = (host[k].to(dev) for k in ("X", "W", "A", "B"))
+    hd, rc = WL["head_dim"], WL["rope_cols"]
+    cos, sin = G.coda_rope_tables(WL["S"], hd, WL["theta"], device=dev)
+    M, K, N = WL["M"], WL["K"], WL["N"]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dP = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused_step(x, w, a_, b_, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        G.coda_gemm_rope(x, w, cos, sin, hd, rc, out=out)
+        if ev is not None:
+            ev[1].record(stream)
+        G.coda_gemm_rope_bwd(a_, b_, cos, sin, hd, rc, out=dP)
+        G.coda_gemm(dP, w, transB=True, out=dX)
+        G.coda_gemm(x, dP, transA=True, out=dW)
+
+    def unfused_step():
+        G.coda_gemm(X, W, out=out)
+        G.coda_unfused_rope(out, cos, sin, hd, rc)
+        G.coda_gemm(A, B, out=dP)
+        G.coda_unfused_rope_bwd(dP, cos, sin, hd, rc)
+        G.coda_gemm(dP, W, transB=True, out=dX)
+        G.coda_gemm(X, dP, transA=True, out=dW)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(step_fn, steps, kernel_events=False):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier()
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step_fn(kev[i] if kernel_events else None)
+            ev[i][1].record(stream)
+        barrier()
+        step_ms = [s.elapsed_time(e) for s, e in ev]
+        k_ms = [s.elapsed_time(e) for s, e in kev] if kernel_events else None
+        return float(np.mean(step_ms)), (float(np.mean(k_ms)) if k_ms else None)
+
+    clocks = Clocks(local)
+    clocks.start()
+    for _ in range(a.warmup):
+        fused_step(X, W, A, B)
+        unfused_step()
+    torch.cuda.synchronize(dev)
+    G.coda_device_status(clear=True)
+
+    ms_fused, ms_rope = timed(lambda ev: fused_step(X, W, A, B, ev), a.steps, kernel_events=True)
+    ms_unfused, _ = timed(lambda ev: unfused_step(), a.steps)
+
+    # end to end through the public API: pinned host inputs -> device, the step,
+    # results back to pinned host memory, all inside each timed step
+    h_out = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    h_dX = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    h_dW = torch.empty((K, N), dtype=torch.bfloat16).pin_memory()
+    dXin = torch.empty_like(X)
+    dWin = torch.empty_like(W)
+    dAin = torch.empty_like(A)
+    dBin = torch.empty_like(B)
+
+    def e2e_step(_ev):
+        dXin.copy_(host["X"], non_blocking=True)
+        dWin.copy_(host["W"], non_blocking=True)
+        dAin.copy_(host["A"], non_blocking=True)
+        dBin.copy_(host["B"], non_blocking=True)
+        fused_step(dXin, dWin, dAin, dBin)
+        h_out.copy_(out, non_blocking=True)
+        h_dX.copy_(dX, non_blocking=True)
+        h_dW.copy_(dW, non_blocking=True)
+
+    e2e_steps = max(3, min(a.steps, 50))
+    for _ in range(2):
+        e2e_step(None)
+    ms_e2e, _ = timed(e2e_step, e2e_steps)
+    clk = clocks.stop()
+    status = G.coda_device_status(clear=True)
+    h2d = sum(host[k].numel() * 2 for k in ("X", "W", "A", "B"))
+    d2h = (M * N + M * K + K * N) * 2
+
+    if dist:
+        t = torch.tensor([ms_fused, ms_unfused, ms_e2e, ms_rope], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_fused, ms_unfused, ms_e2e, ms_rope = (float(v) for v in t.tolist())
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak_tf, _, peak_kind = measured_peaks()
+    achieved = FLOPS_PER_GEMM / (ms_rope * 1e-3) / 1e12
+    traffic = ncu_traffic("coda_gemm_rope")
+    line = {
+        "metric": METRIC,
+        "value": world * FLOPS_PER_STEP / (ms_fused * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": ms_fused,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights, bf16)",
+        "config": config(),
+        "speedup_vs_unfused": ms_unfused / ms_fused,
+        "unfused_ms_per_step": ms_unfused,
+        "pct_bf16_peak": 100.0 * (FLOPS_PER_STEP / (ms_fused * 1e-3) / 1e12) / peak_tf,
+        "clocks": clk,
+        "e2e": {"value": world * FLOPS_PER_STEP / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 4 * a.steps,
+        "roofline": {"kernel": "coda_gemm_rope (gemm_epilogue_kernel<EpiRope<1>>)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}", "traffic": traffic,
+                     "ms_per_launch": ms_rope},
+        "device_status": status,
+    }
+    if not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def reference_arm(a, rank, world):
+    """The float64 CPU oracle on a bounded sample of each step (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import coda_inputs as gen
+    p = gen.rope_problem(WL["M"], WL["K"], WL["N"], seed=0)
+    oracle_prepare(p)
+    rows = calibrate_rows(p, 2.0)
+    for _ in range(a.warmup):
+        oracle_sample(p, rows)
+    ts, fl = [], 0.0
+    for _ in range(a.steps):
+        t, fl = oracle_sample(p, rows)
+        ts.append(t)
+    ms = 1e3 * float(np.mean(ts))
+    value = fl / (ms * 1e-3) / 1e12
+    sample = f"first {rows} of 4096 token rows of each of the 4 GEMMs of one step (float64 NumPy)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same inputs as the GPU arm)",
+        "config": config(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
