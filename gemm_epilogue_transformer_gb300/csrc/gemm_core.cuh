@@ -33,23 +33,34 @@
 
 namespace coda {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int kStages = 4;
+constexpr int BM = 128;       // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;       // accumulator columns per tile
+constexpr int BK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
-constexpr int kABytes = BM * BK * 2;
-constexpr int kBBytes = BN * BK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kStageBoxBytes = 32 * 64;  // one epilogue TMA store box: 32 rows x 64 bytes
 constexpr int kEpiSlots = 2;             // store boxes per staging buffer
 constexpr int kEpiBufs = 2;              // staging double buffer
 constexpr int kEpiWarpBytes = kStageBoxBytes * kEpiSlots * kEpiBufs;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kNumBars * 8 + 16;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Per-variant constants. kCG = 1: one SM computes a 128 x 256 tile. kCG = 2:
+// an SM pair (cta_group::2) computes a 256 x 256 tile; each CTA holds its 128
+// rows of A and half (128 columns) of B, so a stage is 32 KiB per SM instead
+// of 48 KiB and the ring is 6 deep instead of 4.
+template <int kCG>
+struct Cfg {
+  static constexpr int kTileM = BM * kCG;
+  static constexpr int kBLoad = BN / kCG;  // B columns loaded per CTA
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = kBLoad * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kCG == 1 ? 4 : 6;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 struct GemmShape {
   int M, N, K;
@@ -91,7 +102,7 @@ static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t par
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > p.timeout_ns) {
       atomicOr(p.status, CODA_DEVST_TIMEOUT);
@@ -102,13 +113,13 @@ static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t par
 }
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmShape& p,
                                              volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   return wait_bounded_slow(bar, parity, p, abort_flag);
 }
 // Bounded wait used while draining after an abort: ignores the abort flag.
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
   return true;
@@ -163,35 +174,42 @@ __device__ __forceinline__ void load_vec32(const __nv_bfloat16* base, int n, int
 //   __device__ static void store_coord(const Params&, const EpiCtx&, int c, int slot, int& map, int& x, int& y);
 //   __device__ static void end(State&, const Params&, const EpiCtx&);
 // ---------------------------------------------------------------------------
-template <class Epi>
+template <class Epi, int kCG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                          const GemmShape p, const typename Epi::Params ep) {
+  using C = Cfg<kCG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_epi = smem + kStages * kStageBytes;
+  uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_epi + kEpiWarps * kEpiWarpBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t s_base = smem_u32(smem);
+  // In a pair, CTA rank 0 (the leader) issues the MMAs for both; its full and
+  // TMEM-empty barriers collect the pair's arrivals.
+  const uint32_t rank = kCG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x / kCG;
+  const int num_clusters = gridDim.x / kCG;
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
-  auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
-  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
-  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + 2 + b); };
-  const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+  auto empty_bar = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), kEpiWarps * kCG);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -202,65 +220,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kCG == 2) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kCG == 2) cluster_sync_all();  // barriers of both CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (every CTA)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fills[kStages];
+      int fills[C::kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) fills[s] = 0;
+      for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
         int m_blk, n_blk;
         tile_coords(t, p, m_blk, n_blk);
-        const int m0 = m_blk * BM, n0 = n_blk * BN;
+        const int m0 = m_blk * C::kTileM + static_cast<int>(rank) * BM;
+        const int nb0 = n_blk * BN + static_cast<int>(rank) * C::kBLoad;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t a_dst = s_base + stage * kStageBytes;
-          const uint32_t b_dst = a_dst + kABytes;
+          if (leader) mbar_arrive_expect_tx(fb, kCG * C::kStageBytes);
+          const uint32_t fb_target = kCG == 2 ? mapa_shared(fb, 0) : fb;
+          const uint32_t a_dst = s_base + stage * C::kStageBytes;
+          const uint32_t b_dst = a_dst + C::kABytes;
           const int k0 = kb * BK;
+          auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+            if constexpr (kCG == 2)
+              tma_load_2d_pair(dst, m, fb_target, x, y);
+            else
+              tma_load_2d(dst, m, fb_target, x, y);
+          };
           if (p.a_mn) {
-            tma_load_2d(a_dst, &tmA, fb, m0, k0);
-            tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, k0);
+            load(a_dst, &tmA, m0, k0);
+            load(a_dst + 8192, &tmA, m0 + 64, k0);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, k0, m0);
+            load(a_dst, &tmA, k0, m0);
           }
           if (p.b_mn) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < C::kBLoad / 64; ++j) load(b_dst + j * 8192, &tmB, nb0 + 64 * j, k0);
           } else {
-            tma_load_2d(b_dst, &tmB, fb, k0, n0);
+            load(b_dst, &tmB, k0, nb0);
           }
           fills[stage]++;
-          if (++stage == kStages) {
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Drain: every load this thread issued has landed before the CTA exits.
-      for (int s = 0; s < kStages; ++s)
-        if (fills[s] > 0) wait_drain(full_bar(s), static_cast<uint32_t>((fills[s] - 1) & 1), p.timeout_ns);
+      // Drain: every load signalled on this CTA's full barriers has landed
+      // before the CTA exits (in a pair, all loads signal the leader's).
+      if (leader)
+        for (int s = 0; s < C::kStages; ++s)
+          if (fills[s] > 0) wait_drain(full_bar(s), static_cast<uint32_t>((fills[s] - 1) & 1), p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(C::kTileM, BN, p.a_mn, p.b_mn);
       // Operand descriptors. K-major: 128B rows, 8-row groups 1024B apart,
       // K advances 32B (16 bf16) inside the swizzle atom. MN-major: 64-element
       // MN chunks 8192B apart (LBO), 8-row K groups 1024B apart (SBO), K
@@ -271,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++local) {
         const int buf = local & 1;
         const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
         if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, p, abort_flag)) break;
@@ -283,35 +317,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = s_base + stage * kStageBytes;
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t a_addr = s_base + stage * C::kStageBytes;
+          const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024u);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            if constexpr (kCG == 2)
+              tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));
-          if (++stage == kStages) {
+          if constexpr (kCG == 2)
+            tc_commit_pair(empty_bar(stage), 0x3);
+          else
+            tc_commit(empty_bar(stage));
+          if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(buf));
+        if constexpr (kCG == 2)
+          tc_commit_pair(tfull_bar(buf), 0x3);
+        else
+          tc_commit(tfull_bar(buf));
       }
-      // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      tc_commit(drain_bar);
+      // Drain: all MMAs issued here complete before TMEM is freed.
+      if constexpr (kCG == 2)
+        tc_commit_pair(drain_bar, 0x1);
+      else
+        tc_commit(drain_bar);
       wait_drain(drain_bar, 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (every CTA)
     const int ew = warp & 3;
     const uint32_t my_stage = smem_u32(s_epi) + ew * kEpiWarpBytes;
     int local = 0;
     int sbuf = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++local) {
       const int buf = local & 1;
       const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
       if (!wait_bounded(tfull_bar(buf), tphase, p, abort_flag)) break;
@@ -320,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cx.M = p.M;
       cx.N = p.N;
       tile_coords(t, p, cx.m_blk, cx.n_blk);
-      cx.m0 = cx.m_blk * BM;
+      cx.m0 = cx.m_blk * C::kTileM + static_cast<int>(rank) * BM;
       cx.n0 = cx.n_blk * BN;
       cx.n_blocks = p.n_blocks;
       cx.ew = ew;
@@ -363,10 +409,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           sbuf ^= 1;
         }
       }
-      // accumulator buffer fully read: hand it back to the MMA warp
+      // accumulator buffer fully read: hand it back to the MMA issuer
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) {
+        if constexpr (kCG == 2)
+          mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));
+        else
+          mbar_arrive(tempty_bar(buf));
+      }
       Epi::end(st, ep, cx);
     }
     if (lane == 0) bulk_wait_all<0>();
@@ -374,9 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // In a pair, neither CTA releases TMEM (or its shared memory) while the
+  // leader's MMAs may still read or write it.
+  if constexpr (kCG == 2) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kCG == 2)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 

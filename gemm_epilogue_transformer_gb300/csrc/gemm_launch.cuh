@@ -10,7 +10,7 @@
 
 namespace coda {
 
-constexpr int kGroupM = 16;  // row blocks per raster group
+constexpr int kGroupM = 16;  // 128-row blocks per raster group
 
 // Output map for a TMA store target: row-major bf16 [rows, cols], leading
 // dimension ld (elements), 32 x 32 boxes with the 64-byte swizzle.
@@ -19,12 +19,11 @@ inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, in
                        static_cast<uint64_t>(ld) * 2u, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <class Epi>
-int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb,
-                 int b_mn, const CUtensorMap& o0, const CUtensorMap& o1, const typename Epi::Params& ep,
-                 cudaStream_t stream) {
-  const DeviceInfo* di = current_device();
-  if (!di) return CODA_ERR_UNSUPPORTED;
+template <class Epi, int kCG>
+int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, const void* A, int lda, int a_mn,
+                   const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
+                   const typename Epi::Params& ep, cudaStream_t stream) {
+  using C = Cfg<kCG>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
@@ -34,7 +33,8 @@ int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, in
               : make_map_bf16(&tA, A, K, M, static_cast<uint64_t>(lda) * 2u, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     rc = b_mn ? make_map_bf16(&tB, B, N, K, static_cast<uint64_t>(ldb) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-              : make_map_bf16(&tB, B, K, N, static_cast<uint64_t>(ldb) * 2u, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+              : make_map_bf16(&tB, B, K, N, static_cast<uint64_t>(ldb) * 2u, 64, C::kBLoad,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   GemmShape p;
@@ -43,28 +43,66 @@ int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, in
   p.K = K;
   p.a_mn = a_mn;
   p.b_mn = b_mn;
-  p.m_blocks = (M + BM - 1) / BM;
+  p.m_blocks = (M + C::kTileM - 1) / C::kTileM;
   p.n_blocks = (N + BN - 1) / BN;
   p.k_blocks = (K + BK - 1) / BK;
   p.num_tiles = p.m_blocks * p.n_blocks;
-  p.group_m = p.m_blocks < kGroupM ? p.m_blocks : kGroupM;
+  p.group_m = p.m_blocks < kGroupM / kCG ? p.m_blocks : kGroupM / kCG;
   p.status = di->status;
   p.timeout_ns = wait_timeout_ns();
 
-  static int attr_done[64] = {0};
+  auto kernel = &gemm_epilogue_kernel<Epi, kCG>;
+  static int max_clusters[64] = {0};  // per device; 0 = not yet queried
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&gemm_epilogue_kernel<Epi>),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (dev < 0 || dev >= 64) return fail(CODA_ERR_INVALID, "%s: device index %d", fn, dev);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!max_clusters[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-    attr_done[dev] = 1;
+    int n = 0;
+    cfg.gridDim = dim3(kCG, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = di->sm_count / kCG;
+    }
+    max_clusters[dev] = n;
   }
-  const int grid = p.num_tiles < di->sm_count ? p.num_tiles : di->sm_count;
-  gemm_epilogue_kernel<Epi><<<grid, kThreads, kSmemBytes, stream>>>(tA, tB, o0, o1, p, ep);
-  cudaError_t e = cudaGetLastError();
+  const int clusters = p.num_tiles < max_clusters[dev] ? p.num_tiles : max_clusters[dev];
+  cfg.gridDim = dim3(clusters * kCG, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, o0, o1, p, ep);
+  if (e != cudaSuccess) return fail_cuda(e, fn);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, fn);
   return CODA_OK;
+}
+
+// One persistent CTA (kCG = 1) or CTA pair (kCG = 2) per SM / SM pair. The
+// pair variant is used once M spans more than one 128-row block, unless
+// coda_set_cta_group() fixed the choice.
+template <class Epi>
+int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb,
+                 int b_mn, const CUtensorMap& o0, const CUtensorMap& o1, const typename Epi::Params& ep,
+                 cudaStream_t stream) {
+  const DeviceInfo* di = current_device();
+  if (!di) return CODA_ERR_UNSUPPORTED;
+  const int forced = cta_group_setting();
+  const int g = forced ? forced : (M > BM ? 2 : 1);
+  if (g == 2) return launch_variant<Epi, 2>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, ep, stream);
+  return launch_variant<Epi, 1>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, ep, stream);
 }
 
 }  // namespace coda

@@ -23,6 +23,8 @@ struct DeviceInfo {
 // Info for the current device (validated as sm_103); nullptr after fail().
 const DeviceInfo* current_device();
 unsigned long long wait_timeout_ns();
+// 0 = choose per launch, 1 = single-SM tiles, 2 = SM-pair tiles (coda_set_cta_group).
+int cta_group_setting();
 
 // ---------------------------------------------------------------- checks
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

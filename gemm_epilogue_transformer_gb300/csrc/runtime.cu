@@ -13,6 +13,7 @@ namespace coda {
 
 static thread_local char g_err[1024] = "";
 static unsigned long long g_timeout_ns = 2000000000ull;
+static int g_cta_group = 0;
 
 // The device status word (CODA_DEVST_* bits). Kernels receive its device
 // address, obtained per device with cudaGetSymbolAddress.
@@ -75,6 +76,7 @@ const DeviceInfo* current_device() {
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+int cta_group_setting() { return g_cta_group; }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -145,6 +147,12 @@ int coda_device_status(int clear) {
 int coda_set_wait_timeout_ns(unsigned long long ns) {
   if (ns < 100000ull) return fail(CODA_ERR_INVALID, "coda_set_wait_timeout_ns: %llu ns is below 1e5", ns);
   g_timeout_ns = ns;
+  return CODA_OK;
+}
+
+int coda_set_cta_group(int g) {
+  if (g < 0 || g > 2) return fail(CODA_ERR_INVALID, "coda_set_cta_group: %d is not 0, 1 or 2", g);
+  g_cta_group = g;
   return CODA_OK;
 }
 

@@ -74,6 +74,13 @@ int coda_device_status(int clear);
  * Values below 1e5 are rejected with CODA_ERR_INVALID. */
 int coda_set_wait_timeout_ns(unsigned long long ns);
 
+/* GEMM tile variant for every later launch on this process: 1 = one SM per
+ * 128 x 256 tile (tcgen05 cta_group::1); 2 = an SM pair per 256 x 256 tile
+ * (cta_group::2, 2-CTA clusters); 0 (default) = the pair whenever M > 128.
+ * Results are identical up to fp32 accumulation order. Other values are
+ * rejected with CODA_ERR_INVALID. */
+int coda_set_cta_group(int g);
+
 /* Number of column tiles of a fused kernel's output for GEMM width N
  * (ceil(N / 256)): the second dimension of every [M, nb] partial buffer. */
 int coda_num_col_tiles(int N);

@@ -28,8 +28,16 @@ def _dev_f32(a):
 
 # ---------------------------------------------------------------- RMSNorm chain
 
+@pytest.fixture(params=[0, 1], ids=["auto", "cta1"])
+def cta_group(coda, request):
+    """Automatic tile choice (SM pairs once M > 128) and forced single-SM tiles."""
+    coda.coda_set_cta_group(request.param)
+    yield request.param
+    coda.coda_set_cta_group(0)
+
+
 @pytest.mark.parametrize("M,K,d,N2", [(256, 512, 512, 512), (300, 200, 520, 264), (1, 64, 8, 8)])
-def test_rms_chain_forward(coda, M, K, d, N2):
+def test_rms_chain_forward(coda, cta_group, M, K, d, N2):
     p = gen.rms_chain(M, K, d, N2, seed=0)
     x, W0, z, g, W1 = (p[k] for k in ("x", "W0", "z", "gamma", "W1"))
     h1, h2, psq = coda.coda_gemm_res_rmsprep(dev_bf16(x), dev_bf16(W0), dev_bf16(z), dev_bf16(g))
@@ -61,7 +69,7 @@ def test_rms_chain_k_zero(coda):
     assert_stat(f64(psq).sum(axis=1), np.sum(O.bf16(p["z"]) ** 2, axis=1), "psq K=0")
 
 
-def test_rms_chain_backward(coda):
+def test_rms_chain_backward(coda, cta_group):
     M, K, d, N2, Kn = 300, 200, 264, 520, 136
     p = gen.rms_chain(M, K, d, N2, seed=1, bwd_K=Kn)
     x, W0, z, g, W1 = (p[k] for k in ("x", "W0", "z", "gamma", "W1"))

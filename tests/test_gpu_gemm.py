@@ -28,9 +28,17 @@ def _operands(M, N, K, ta, tb, seed):
     return A, B
 
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+def cta_group(coda, request):
+    """Run the test with the single-SM (128 x 256) and the SM-pair (256 x 256) tile variant."""
+    coda.coda_set_cta_group(request.param)
+    yield request.param
+    coda.coda_set_cta_group(0)
+
+
 @pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_gemm_parity(coda, M, N, K, ta, tb):
+def test_gemm_parity(coda, cta_group, M, N, K, ta, tb):
     if ta and M % 8:
         pytest.skip("transposed A needs M % 8 == 0 (16-byte rows)")
     A, B = _operands(M, N, K, ta, tb, seed=M * 7 + N * 3 + K + ta * 2 + tb)
@@ -40,7 +48,7 @@ def test_gemm_parity(coda, M, N, K, ta, tb):
     assert_bf16(f64(C), O.matmul(a, b), f"gemm {M}x{N}x{K} ta={ta} tb={tb}")
 
 
-def test_gemm_k_zero_and_empty(coda):
+def test_gemm_k_zero_and_empty(coda, cta_group):
     import torch
     A = torch.zeros((16, 0), dtype=torch.bfloat16, device="cuda")
     B = torch.zeros((0, 24), dtype=torch.bfloat16, device="cuda")
@@ -52,7 +60,7 @@ def test_gemm_k_zero_and_empty(coda):
     assert E.shape == (0, 16)
 
 
-def test_gemm_leading_dims(coda):
+def test_gemm_leading_dims(coda, cta_group):
     """Row strides larger than the logical width (views into wider buffers)."""
     M, N, K = 200, 136, 72
     A, B = _operands(M, N + 24, K + 40, 0, 0, seed=5)
