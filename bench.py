@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--suite", action="store_true",
+                    help="time every fused operator against its unfused pair on all five workloads "
+                         "(one JSON line per operator) instead of the headline step")
+    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite")
     return ap.parse_args()
 
 
@@ -186,6 +190,8 @@ def main():
     import coda_inputs as gen
     if a.impl == "reference":
         return reference_arm(a, rank, world)
+    if a.suite:
+        return suite(a)
 
     import torch
     torch.cuda.set_device(local)
@@ -373,6 +379,153 @@ def reference_arm(a, rank, world):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------- operator suite
+
+def suite(a):
+    """Fused vs unfused time of every operator on the five workloads; one JSON line each."""
+    import torch
+    import coda_inputs as gen
+    from gemm_epilogue_transformer_gb300 import build_lib
+    build_lib.build()
+    import gemm_epilogue_transformer_gb300 as G
+    G.coda_init(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    peak_tf, peak_bw, peak_kind = measured_peaks()
+
+    def d(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def t_ms(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(a.reps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            e.synchronize()
+            ts.append(s.elapsed_time(e))
+        return float(np.median(ts)), float(np.min(ts))
+
+    def report(workload, op, flops, fused, unfused, launches):
+        fm, fmin = t_ms(fused)
+        um, umin = t_ms(unfused)
+        line = {"suite": workload, "op": op, "fused_ms": fm, "fused_min_ms": fmin, "unfused_ms": um,
+                "unfused_min_ms": umin, "speedup_vs_unfused": um / fm,
+                "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None,
+                "pct_bf16_peak": 100 * flops / (fm * 1e-3) / 1e12 / peak_tf if flops else None,
+                "kernels": launches, "peak": f"{peak_tf} TFLOP/s ({peak_kind})", "reps": a.reps}
+        print(json.dumps(line), flush=True)
+
+    # -- GEMM-RMSNorm-GEMM (tiny and 8192)
+    for name, M, Kd, bwdK in (("rmsnorm_chain_tiny", 256, 512, 512), ("rmsnorm_chain_8192", 8192, 8192, 8192)):
+        p = gen.rms_chain(M, Kd, Kd, Kd, seed=0, bwd_K=bwdK)
+        x, W0, z, g, W1, dO, Wn = (d(p[k]) for k in ("x", "W0", "z", "gamma", "W1", "dO", "Wn"))
+        d_ = Kd
+        nb = G.coda_num_col_tiles(d_)
+        h1 = torch.empty((M, d_), dtype=torch.bfloat16, device=dev)
+        h2, h0, n, Y, dY, dYr, Gm, dh1 = (torch.empty_like(h1) for _ in range(8))
+        psq = torch.empty((M, nb), dtype=torch.float32, device=dev)
+        pdot = torch.empty_like(psq)
+        r = torch.empty((M,), dtype=torch.float32, device=dev)
+        ru = torch.empty_like(r)
+
+        def fused_fwd():
+            G.coda_gemm_res_rmsprep(x, W0, z, g, h1=h1, h2=h2, psq=psq)
+            G.coda_rms_reduce(psq, d_, 1e-6, r=r)
+            G.coda_gemm_rowscale(h2, W1, r, out=Y)
+
+        def unfused_fwd():
+            G.coda_gemm(x, W0, out=h0)
+            G.coda_unfused_add(h0, z, out=h1)
+            nn, rr = G.coda_unfused_rmsnorm(h1, g, 1e-6)
+            G.coda_gemm(nn, W1, out=Y)
+
+        report(name, "fwd", 2 * 2.0 * M * Kd * d_, fused_fwd, unfused_fwd, "3 fused (2 GEMM + aux) vs 4 unfused")
+        fused_fwd()
+
+        def fused_bwd():
+            dY_, dYr_, pd = G.coda_gemm_rowdot(dO, Wn, Y, r)
+            s_ = G.coda_rowdot_reduce(pd, d_)
+            dh, pdg = G.coda_gemm_rmsnorm_bwd(dY_, W1, h1, g, r, s_)
+            G.coda_colsum_reduce(pdg)
+
+        def unfused_bwd():
+            dY_ = G.coda_gemm(dO, Wn)
+            Gd = G.coda_gemm(dY_, W1, transB=True)
+            dh, pdg = G.coda_unfused_rmsnorm_bwd(Gd, h1, g, r)
+            G.coda_colsum_reduce(pdg)
+
+        report(name, "bwd", 2 * 2.0 * M * Kd * d_, fused_bwd, unfused_bwd,
+               "dY GEMM + rowdot + RMSNorm-bwd GEMM + 2 aux vs 2 GEMM + rmsnorm_bwd + colsum")
+        del p, x, W0, z, g, W1, dO, Wn, h1, h2, h0, n, Y, dY, dYr, Gm, dh1
+        torch.cuda.empty_cache()
+
+    # -- GEMM + RoPE
+    M, K, N, hd, rc = 4096, 4096, 12288, 128, 8192
+    p = gen.rope_problem(M, K, N, seed=0)
+    X, W, A_, B_ = (d(p[k]) for k in ("X", "W", "A", "B"))
+    c, sn = G.coda_rope_tables(4096, hd, 10000.0, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    report("rope_qkv_4096", "fwd", 2.0 * M * N * K, lambda: G.coda_gemm_rope(X, W, c, sn, hd, rc, out=out),
+           lambda: (G.coda_gemm(X, W, out=out), G.coda_unfused_rope(out, c, sn, hd, rc)), "1 vs 2")
+    report("rope_qkv_4096", "bwd", 2.0 * M * N * K, lambda: G.coda_gemm_rope_bwd(A_, B_, c, sn, hd, rc, out=out),
+           lambda: (G.coda_gemm(A_, B_, out=out), G.coda_unfused_rope_bwd(out, c, sn, hd, rc)), "1 vs 2")
+    report("rope_qkv_4096", "plain_gemm", 2.0 * M * N * K, lambda: G.coda_gemm(X, W, out=out),
+           lambda: G.coda_gemm(X, W, out=out), "identity epilogue, both columns the same kernel")
+    del p, X, W, A_, B_, out
+    torch.cuda.empty_cache()
+
+    # -- GEMM + SwiGLU
+    M, K, F = 4096, 4096, 14336
+    p = gen.swiglu_problem(M, K, F, seed=0)
+    X, Wgu, dYs, Wd = (d(p[k]) for k in ("X", "Wgu", "dY", "Wd"))
+    A = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
+    GU = torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev)
+    dA = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
+    dGU = torch.empty_like(GU)
+    report("swiglu_up_4096", "fwd", 2.0 * M * 2 * F * K, lambda: G.coda_gemm_swiglu(X, Wgu, out=A),
+           lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (no GU saved)")
+    report("swiglu_up_4096", "fwd_save_gu", 2.0 * M * 2 * F * K,
+           lambda: G.coda_gemm_swiglu(X, Wgu, out=A, gu=GU),
+           lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (GU saved for backward)")
+    report("swiglu_up_4096", "bwd", 2.0 * M * F * K, lambda: G.coda_gemm_swiglu_bwd(dYs, Wd, GU, out=dGU),
+           lambda: (G.coda_gemm(dYs, Wd, transB=True, out=dA), G.coda_unfused_swiglu_bwd(dA, GU)), "1 vs 2")
+    del p, X, Wgu, dYs, Wd, A, GU, dA, dGU
+    torch.cuda.empty_cache()
+
+    # -- LM head + cross-entropy
+    M, K, V = 8192, 4096, 32768
+    p = gen.ce_problem(M, K, V, seed=0)
+    H, W = d(p["H"]), d(p["W"])
+    y = torch.from_numpy(p["labels"]).to(dev)
+    logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    st = {}
+
+    def fused_ce():
+        pm, ps, pa, tg = G.coda_gemm_ce_lse(H, W, y)
+        st["lse"] = G.coda_ce_reduce(pm, ps, pa, tg)[0]
+
+    def unfused_ce():
+        G.coda_gemm(H, W, out=logits)
+        G.coda_unfused_ce_fwd(logits, y)
+
+    report("lm_head_ce_8192", "fwd", 2.0 * M * V * K, fused_ce, unfused_ce, "GEMM+partials + reduce vs GEMM (bf16 logits) + CE")
+    fused_ce()
+    lse = st["lse"]
+    report("lm_head_ce_8192", "bwd_dlogits", 2.0 * M * V * K,
+           lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
+           lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
+           "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel")
+    status = G.coda_device_status(clear=True)
+    print(json.dumps({"suite": "done", "device_status": status}), flush=True)
+    return 0 if status == 0 else 1
 
 
 if __name__ == "__main__":
