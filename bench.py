@@ -51,6 +51,9 @@ def parse():
                     help="time every fused operator against its unfused pair on all five workloads "
                          "(one JSON line per operator) instead of the headline step")
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite")
+    ap.add_argument("--only", default=None,
+                    help="with --suite: run one workload (rmsnorm_chain_tiny, rmsnorm_chain_8192, rope_qkv_4096, "
+                         "swiglu_up_4096, lm_head_ce_8192)")
     return ap.parse_args()
 
 
@@ -424,7 +427,12 @@ def suite(a):
         print(json.dumps(line), flush=True)
 
     # -- GEMM-RMSNorm-GEMM (tiny and 8192)
+    def want(name):
+        return a.only is None or a.only == name
+
     for name, M, Kd, bwdK in (("rmsnorm_chain_tiny", 256, 512, 512), ("rmsnorm_chain_8192", 8192, 8192, 8192)):
+        if not want(name):
+            continue
         p = gen.rms_chain(M, Kd, Kd, Kd, seed=0, bwd_K=bwdK)
         x, W0, z, g, W1, dO, Wn = (d(p[k]) for k in ("x", "W0", "z", "gamma", "W1", "dO", "Wn"))
         d_ = Kd
@@ -469,6 +477,19 @@ def suite(a):
 
     # -- GEMM + RoPE
     M, K, N, hd, rc = 4096, 4096, 12288, 128, 8192
+    if want("rope_qkv_4096"):
+        rope_suite(G, gen, d, dev, report, M, K, N, hd, rc)
+    if want("swiglu_up_4096"):
+        swiglu_suite(G, gen, d, dev, report)
+    if want("lm_head_ce_8192"):
+        ce_suite(G, gen, d, dev, report)
+    status = G.coda_device_status(clear=True)
+    print(json.dumps({"suite": "done", "device_status": status}), flush=True)
+    return 0 if status == 0 else 1
+
+
+def rope_suite(G, gen, d, dev, report, M, K, N, hd, rc):
+    import torch
     p = gen.rope_problem(M, K, N, seed=0)
     X, W, A_, B_ = (d(p[k]) for k in ("X", "W", "A", "B"))
     c, sn = G.coda_rope_tables(4096, hd, 10000.0, device=dev)
@@ -482,7 +503,9 @@ def suite(a):
     del p, X, W, A_, B_, out
     torch.cuda.empty_cache()
 
-    # -- GEMM + SwiGLU
+
+def swiglu_suite(G, gen, d, dev, report):
+    import torch
     M, K, F = 4096, 4096, 14336
     p = gen.swiglu_problem(M, K, F, seed=0)
     X, Wgu, dYs, Wd = (d(p[k]) for k in ("X", "Wgu", "dY", "Wd"))
@@ -500,7 +523,9 @@ def suite(a):
     del p, X, Wgu, dYs, Wd, A, GU, dA, dGU
     torch.cuda.empty_cache()
 
-    # -- LM head + cross-entropy
+
+def ce_suite(G, gen, d, dev, report):
+    import torch
     M, K, V = 8192, 4096, 32768
     p = gen.ce_problem(M, K, V, seed=0)
     H, W = d(p["H"]), d(p["W"])
@@ -523,9 +548,6 @@ def suite(a):
            lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
            lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
            "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel")
-    status = G.coda_device_status(clear=True)
-    print(json.dumps({"suite": "done", "device_status": status}), flush=True)
-    return 0 if status == 0 else 1
 
 
 if __name__ == "__main__":

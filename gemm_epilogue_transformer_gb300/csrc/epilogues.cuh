@@ -16,7 +16,36 @@ namespace coda {
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float exp_f(float x) { return exp2f(x * kLog2e); }
-__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + exp_f(-g)); }
+// 1 / (1 + e^-g) with the fast reciprocal-multiply division (about 2 ulp);
+// for g below about -88 the denominator overflows and the result is 0, the
+// correct limit.
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + exp_f(-g)); }
+
+// Epilogues without global inputs carry an empty prefetch buffer.
+struct NoPre {
+  uint32_t unused;
+};
+#define CODA_NO_PREFETCH                                                            \
+  using Pre = NoPre;                                                                \
+  __device__ static void prefetch(const Params&, const EpiCtx&, int, Pre&) {}
+#define CODA_NO_INPUT                                                                                   \
+  static constexpr int kInBoxes = 0;                                                                    \
+  __device__ static bool has_input(const Params&, const EpiCtx&, int) { return false; }                 \
+  __device__ static void in_coord(const Params&, const EpiCtx&, int, int, int& map, int& x, int& y) {  \
+    map = 0;                                                                                            \
+    x = 0;                                                                                              \
+    y = 0;                                                                                              \
+  }
+// One bf16 input box per chunk: the 32 x 32 block of a [M, N] tensor under the
+// warp's rows and the chunk's columns.
+#define CODA_INPUT_SAME_TILE                                                                             \
+  static constexpr int kInBoxes = 1;                                                                     \
+  __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }                   \
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) { \
+    map = 0;                                                                                             \
+    x = cx.n0 + 32 * c;                                                                                  \
+    y = cx.wrow0;                                                                                        \
+  }
 
 // Sum each of the 32 columns held by the warp's 32 rows; afterwards lane j
 // holds the total of column j in v[0]. 31 shuffles per thread.
@@ -48,11 +77,13 @@ struct EpiPlain {
     int unused;
   };
   struct State {};
+  CODA_NO_PREFETCH
+  CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], uint32_t box0,
-                               uint32_t) {
+  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&, uint32_t,
+                               uint32_t box0, uint32_t) {
     stage_row32(box0, cx.lane, acc);
   }
   CODA_STORE_SAME_COLS(0)
@@ -71,21 +102,29 @@ struct EpiResRmsPrep {
   struct State {
     float sumsq;
   };
+  struct Pre {
+    uint4 g[4];
+  };
+  __device__ static void prefetch(const Params& ep, const EpiCtx& cx, int c, Pre& pr) {
+    load_raw32(ep.gamma, 0, 1, cx.N, 0, cx.n0 + 32 * c, pr.g);
+  }
+  CODA_INPUT_SAME_TILE  // z
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params&, const EpiCtx&) { st.sumsq = 0.f; }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
-                               uint32_t box0, uint32_t box1) {
-    const int col0 = cx.n0 + 32 * c;
+  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre& pr,
+                               uint32_t in, uint32_t box0, uint32_t box1) {
     float v[32];
-    load_row32(ep.z, cx.N, cx.M, cx.N, cx.row, col0, v);
+    uint4 u[4];
+    box_row(in, cx.lane, u);
+    unpack32(u, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       acc[i] += v[i];
       st.sumsq = fmaf(acc[i], acc[i], st.sumsq);
     }
     stage_row32(box0, cx.lane, acc);
-    load_vec32(ep.gamma, cx.N, col0, v);
+    unpack32(pr.g, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] *= v[i];
     stage_row32(box1, cx.lane, acc);
@@ -105,13 +144,15 @@ struct EpiRowScale {
   struct State {
     float rv;
   };
+  CODA_NO_PREFETCH
+  CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
   }
-  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], uint32_t box0,
-                               uint32_t) {
+  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
+                               uint32_t, uint32_t box0, uint32_t) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] *= st.rv;
     stage_row32(box0, cx.lane, acc);
@@ -130,11 +171,13 @@ struct EpiSwiGLU {
     __nv_bfloat16* gu;  // nullable, [M, 2F]
   };
   struct State {};
+  CODA_NO_PREFETCH
+  CODA_NO_INPUT
   static constexpr int kChunksPerStore = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t box0,
-                               uint32_t) {
+  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
+                               uint32_t, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
     if (ep.gu != nullptr && cx.row < cx.M) {
       uint4* dst = reinterpret_cast<uint4*>(ep.gu + static_cast<long>(cx.row) * cx.N + col0);
@@ -173,17 +216,26 @@ struct EpiSwiGLUBwd {
     const __nv_bfloat16* gu;  // [M, 2F]
   };
   struct State {};
+  CODA_NO_PREFETCH
+  // the 64 interleaved GU columns of the chunk's 32 gate/up pairs: two boxes
+  static constexpr int kInBoxes = 2;
+  __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+    map = 0;
+    x = 2 * (cx.n0 + 32 * c) + 32 * b;
+    y = cx.wrow0;
+  }
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t box0,
-                               uint32_t box1) {
-    const int f0 = cx.n0 + 32 * c;
-    const int ld = 2 * cx.N;
+  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
+                               uint32_t in, uint32_t box0, uint32_t box1) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float g[32];
-      load_row32(ep.gu, ld, cx.M, ld, cx.row, 2 * f0 + 32 * half, g);
+      uint4 u[4];
+      box_row(in + half * kInBoxBytes, cx.lane, u);
+      unpack32(u, g);
       float o[32];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
@@ -213,28 +265,61 @@ struct EpiRope {
     const float* cos_tab;
     const float* sin_tab;
     int S, head_dim, rope_cols;
+    int tma_tables;  // 1: the cos/sin slices arrive by TMA (S % 32 == 0); 0: direct loads
   };
-  struct State {
-    int pos;
+  struct State {};
+  struct Pre {
+    uint4 c[4], s[4];
   };
-  static constexpr int kChunksPerStore = 1;
-  __device__ static int slots(const Params&) { return 1; }
-  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    st.pos = (cx.row < cx.M) ? (cx.row % ep.S) : 0;
+  // With S % 32 == 0 a warp's 32 rows are 32 consecutive positions, so the
+  // chunk's 16 cos and 16 sin columns are one 32 x 64B fp32 box each.
+  static constexpr int kInBoxes = 2;
+  __device__ static bool has_input(const Params& ep, const EpiCtx& cx, int c) {
+    return ep.tma_tables && cx.n0 + 32 * c < ep.rope_cols;
   }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
-                               uint32_t box0, uint32_t) {
+  __device__ static void in_coord(const Params& ep, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+    map = b;
+    x = ((cx.n0 + 32 * c) % ep.head_dim) >> 1;
+    y = cx.wrow0 % ep.S;
+  }
+  __device__ static void prefetch(const Params& ep, const EpiCtx& cx, int c, Pre& pr) {
     const int col0 = cx.n0 + 32 * c;
-    if (col0 < ep.rope_cols) {
+    if (!ep.tma_tables && col0 < ep.rope_cols) {
+      const int pos = (cx.row < cx.M) ? (cx.row % ep.S) : 0;
       const int half = ep.head_dim >> 1;
       const int i0 = (col0 % ep.head_dim) >> 1;
-      const float* cp = ep.cos_tab + static_cast<long>(st.pos) * half + i0;
-      const float* sp = ep.sin_tab + static_cast<long>(st.pos) * half + i0;
-      float cs[16], sn[16];
+      const float* cp = ep.cos_tab + static_cast<long>(pos) * half + i0;
+      const float* sp = ep.sin_tab + static_cast<long>(pos) * half + i0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 a = ldg_nc_v4(cp + 4 * q);
-        const uint4 b = ldg_nc_v4(sp + 4 * q);
+        pr.c[q] = ldg_nc_v4(cp + 4 * q);
+        pr.s[q] = ldg_nc_v4(sp + 4 * q);
+      }
+    }
+  }
+  static constexpr int kChunksPerStore = 1;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
+  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
+                               uint32_t in, uint32_t box0, uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    if (col0 < ep.rope_cols) {
+      float cs[16], sn[16];
+      uint4 tc[4], ts[4];
+      if (in) {
+        box_row(in, cx.lane, tc);
+        box_row(in + kInBoxBytes, cx.lane, ts);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tc[q] = pr.c[q];
+          ts[q] = pr.s[q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 a = tc[q];
+        const uint4 b = ts[q];
         cs[4 * q + 0] = __uint_as_float(a.x);
         cs[4 * q + 1] = __uint_as_float(a.y);
         cs[4 * q + 2] = __uint_as_float(a.z);
@@ -276,6 +361,8 @@ struct EpiCeLse {
     int best;
     int label;
   };
+  CODA_NO_PREFETCH
+  CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 0; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
@@ -291,8 +378,8 @@ struct EpiCeLse {
       }
     }
   }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], uint32_t,
-                               uint32_t) {
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
+                               uint32_t, uint32_t, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
     float cm = -INFINITY;
     int ci = 0;
@@ -349,14 +436,16 @@ struct EpiCeBwd {
     int label;
     float lse;
   };
+  CODA_NO_PREFETCH
+  CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.label = (cx.row < cx.M) ? ep.labels[cx.row] : -1;
     st.lse = (cx.row < cx.M) ? ep.lse[cx.row] : 0.f;
   }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
-                               uint32_t box0, uint32_t) {
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
+                               uint32_t, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -383,16 +472,20 @@ struct EpiRowdot {
   struct State {
     float dot, rv;
   };
+  CODA_NO_PREFETCH
+  CODA_INPUT_SAME_TILE  // Y
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params& ep) { return ep.store_dyr ? 2 : 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = 0.f;
     st.rv = (ep.store_dyr && cx.row < cx.M) ? ep.r[cx.row] : 0.f;
   }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
-                               uint32_t box0, uint32_t box1) {
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
+                               uint32_t in, uint32_t box0, uint32_t box1) {
     float y[32];
-    load_row32(ep.Y, cx.N, cx.M, cx.N, cx.row, cx.n0 + 32 * c, y);
+    uint4 u[4];
+    box_row(in, cx.lane, u);
+    unpack32(u, y);
 #pragma unroll
     for (int i = 0; i < 32; ++i) st.dot = fmaf(acc[i], y[i], st.dot);
     stage_row32(box0, cx.lane, acc);
@@ -422,6 +515,13 @@ struct EpiRmsNormBwd {
   struct State {
     float rv, r2s;
   };
+  struct Pre {
+    uint4 g[4];
+  };
+  __device__ static void prefetch(const Params& ep, const EpiCtx& cx, int c, Pre& pr) {
+    load_raw32(ep.gamma, 0, 1, cx.N, 0, cx.n0 + 32 * c, pr.g);
+  }
+  CODA_INPUT_SAME_TILE  // h1
   static constexpr int kChunksPerStore = 1;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
@@ -433,12 +533,14 @@ struct EpiRmsNormBwd {
       st.r2s = 0.f;
     }
   }
-  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32],
-                               uint32_t box0, uint32_t) {
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
+                               uint32_t in, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
     float h[32], g[32], part[32];
-    load_row32(ep.h1, cx.N, cx.M, cx.N, cx.row, col0, h);
-    load_vec32(ep.gamma, cx.N, col0, g);
+    uint4 u[4];
+    box_row(in, cx.lane, u);
+    unpack32(u, h);
+    unpack32(pr.g, g);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       part[i] = st.rv * acc[i] * h[i];

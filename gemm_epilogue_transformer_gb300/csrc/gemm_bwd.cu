@@ -33,9 +33,11 @@ int coda_gemm_swiglu_bwd(int M, int F, int K, const coda_bf16* dY, const coda_bf
   CODA_REQ_PTR16(dgu_out);
   CUtensorMap o;
   if ((rc = make_out_map(&o, dgu_out, M, 2 * F, 2 * F))) return rc;
+  CUtensorMap ig;
+  if ((rc = make_out_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
   EpiSwiGLUBwd::Params ep{reinterpret_cast<const __nv_bfloat16*>(gu)};
   // dA = dY Wd^T: Wd is stored [F, K] = [N, K], a K-major B operand.
-  return launch_fused<EpiSwiGLUBwd>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ep, as_stream(stream));
+  return launch_fused<EpiSwiGLUBwd>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, ep, as_stream(stream));
 }
 
 int coda_gemm_rowdot(int M, int N, int K, const coda_bf16* dO, const coda_bf16* Wn, const coda_bf16* Y,
@@ -56,8 +58,10 @@ int coda_gemm_rowdot(int M, int N, int K, const coda_bf16* dO, const coda_bf16* 
   } else {
     o1 = o0;
   }
+  CUtensorMap iy;
+  if ((rc = make_out_map(&iy, Y, M, N, N))) return rc;
   EpiRowdot::Params ep{reinterpret_cast<const __nv_bfloat16*>(Y), r, pdot_out, dYr_out != nullptr};
-  return launch_fused<EpiRowdot>(fn, M, N, K, dO, K, 0, Wn, N, /*b_mn=*/1, o0, o1, ep, as_stream(stream));
+  return launch_fused<EpiRowdot>(fn, M, N, K, dO, K, 0, Wn, N, /*b_mn=*/1, o0, o1, iy, iy, ep, as_stream(stream));
 }
 
 int coda_gemm_rmsnorm_bwd(int M, int d, int K, const coda_bf16* dY, const coda_bf16* W1, const coda_bf16* h1,
@@ -75,10 +79,12 @@ int coda_gemm_rmsnorm_bwd(int M, int d, int K, const coda_bf16* dY, const coda_b
   CODA_REQ_PTR4(pdg_out);
   CUtensorMap o;
   if ((rc = make_out_map(&o, dh1_out, M, d, d))) return rc;
+  CUtensorMap ih;
+  if ((rc = make_out_map(&ih, h1, M, d, d))) return rc;
   EpiRmsNormBwd::Params ep{reinterpret_cast<const __nv_bfloat16*>(h1), reinterpret_cast<const __nv_bfloat16*>(gamma),
                            r, s, pdg_out};
   // G = dY W1^T: W1 is stored [d, K] = [N, K], a K-major B operand.
-  return launch_fused<EpiRmsNormBwd>(fn, M, d, K, dY, K, 0, W1, K, /*b_mn=*/0, o, o, ep, as_stream(stream));
+  return launch_fused<EpiRmsNormBwd>(fn, M, d, K, dY, K, 0, W1, K, /*b_mn=*/0, o, o, ih, ih, ep, as_stream(stream));
 }
 
 int coda_gemm_ce_lse(int M, int V, int K, const coda_bf16* H, const coda_bf16* W, const int32_t* labels,
@@ -98,7 +104,7 @@ int coda_gemm_ce_lse(int M, int V, int K, const coda_bf16* H, const coda_bf16* W
   CUtensorMap o;
   memset(&o, 0, sizeof(o));
   EpiCeLse::Params ep{labels, pmax_out, psum_out, parg_out, tgt_out, di->status};
-  return launch_fused<EpiCeLse>(fn, M, V, K, H, K, 0, W, V, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  return launch_fused<EpiCeLse>(fn, M, V, K, H, K, 0, W, V, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 int coda_gemm_ce_bwd(int M, int V, int K, const coda_bf16* H, const coda_bf16* W, const int32_t* labels,
@@ -113,7 +119,7 @@ int coda_gemm_ce_bwd(int M, int V, int K, const coda_bf16* H, const coda_bf16* W
   CUtensorMap o;
   if ((rc = make_out_map(&o, dl_out, M, V, V))) return rc;
   EpiCeBwd::Params ep{labels, lse, grad_scale};
-  return launch_fused<EpiCeBwd>(fn, M, V, K, H, K, 0, W, V, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  return launch_fused<EpiCeBwd>(fn, M, V, K, H, K, 0, W, V, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 }  // extern "C"

@@ -43,23 +43,33 @@ constexpr int kStageBoxBytes = 32 * 64;  // one epilogue TMA store box: 32 rows 
 constexpr int kEpiSlots = 2;             // store boxes per staging buffer
 constexpr int kEpiBufs = 2;              // staging double buffer
 constexpr int kEpiWarpBytes = kStageBoxBytes * kEpiSlots * kEpiBufs;
+// Rank-2 epilogue inputs (z, Y, h1, GU, RoPE tables) arrive by TMA in 32 x 64B
+// boxes into a per-warp ring of kInWarpBytes, issued several chunks ahead.
+constexpr int kInBoxBytes = 32 * 64;
+constexpr int kInWarpBytes = 8192;
+constexpr int kMaxInSlots = 4;
 
 // Per-variant constants. kCG = 1: one SM computes a 128 x 256 tile. kCG = 2:
 // an SM pair (cta_group::2) computes a 256 x 256 tile; each CTA holds its 128
 // rows of A and half (128 columns) of B, so a stage is 32 KiB per SM instead
-// of 48 KiB and the ring is 6 deep instead of 4.
-template <int kCG>
+// of 48 KiB and the ring is 6 deep instead of 4. kIn = input boxes per chunk
+// (0, 1, 2): epilogues with inputs give one mainloop stage to the input ring
+// (a 5-deep ring measured as fast as a 6-deep one for the pair variant).
+template <int kCG, int kIn>
 struct Cfg {
   static constexpr int kTileM = BM * kCG;
   static constexpr int kBLoad = BN / kCG;  // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = kBLoad * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kCG == 1 ? 4 : 6;
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+  static constexpr int kStages = kCG == 1 ? (kIn ? 3 : 4) : (kIn ? 5 : 6);
+  static constexpr int kInSlots = kIn ? kInWarpBytes / (kIn * kInBoxBytes) : 0;
+  static constexpr int kInBytes = kIn ? kEpiWarps * kInWarpBytes : 0;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kNumBars * 8 + 16;
+      1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kInSlots <= kMaxInSlots, "input ring slots");
 };
 
 struct GemmShape {
@@ -139,38 +149,53 @@ __device__ __forceinline__ void stage_row32(uint32_t box, int r, const float (&v
               pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
-// Load 32 consecutive bf16 of a row-major [rows, cols] tensor starting at
-// (row, col0) as fp32; elements past the bounds read as 0. cols is a multiple
-// of 8, col0 a multiple of 32, so each 16-byte vector is all-in or all-out.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* base, long ld, int rows, int cols, int row, int col0,
-                                           float (&v)[32]) {
+// Row r (0..31) of a 32 x 64B box laid out with the TMA 64-byte swizzle, as
+// four 16-byte vectors (conflict-free across the warp).
+__device__ __forceinline__ void box_row(uint32_t box, int r, uint4 (&v)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = ld_shared_v4(box + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+
+// Issue the loads of 32 consecutive bf16 of a row-major [rows, cols] tensor
+// starting at (row, col0) as four 16-byte vectors; vectors past the bounds are
+// zero. cols is a multiple of 8 and col0 of 32, so each vector is all-in or
+// all-out. The values are consumed later (unpack32), so the load latency
+// overlaps whatever runs in between.
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* base, long ld, int rows, int cols, int row, int col0,
+                                           uint4 (&v)[4]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (row < rows && col0 + 8 * q < cols) u = ldg_nc_v4(base + static_cast<long>(row) * ld + col0 + 8 * q);
-    v[8 * q + 0] = bf16_lo(u.x);
-    v[8 * q + 1] = bf16_hi(u.x);
-    v[8 * q + 2] = bf16_lo(u.y);
-    v[8 * q + 3] = bf16_hi(u.y);
-    v[8 * q + 4] = bf16_lo(u.z);
-    v[8 * q + 5] = bf16_hi(u.z);
-    v[8 * q + 6] = bf16_lo(u.w);
-    v[8 * q + 7] = bf16_hi(u.w);
+    v[q] = make_uint4(0, 0, 0, 0);
+    if (row < rows && col0 + 8 * q < cols) v[q] = ldg_nc_v4(base + static_cast<long>(row) * ld + col0 + 8 * q);
   }
 }
-// 32 consecutive bf16 of a vector (same address for the whole warp: broadcast).
-__device__ __forceinline__ void load_vec32(const __nv_bfloat16* base, int n, int col0, float (&v)[32]) {
-  load_row32(base, 0, 1, n, 0, col0, v);
+__device__ __forceinline__ void unpack32(const uint4 (&u)[4], float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[8 * q + 0] = bf16_lo(u[q].x);
+    v[8 * q + 1] = bf16_hi(u[q].x);
+    v[8 * q + 2] = bf16_lo(u[q].y);
+    v[8 * q + 3] = bf16_hi(u[q].y);
+    v[8 * q + 4] = bf16_lo(u[q].z);
+    v[8 * q + 5] = bf16_hi(u[q].z);
+    v[8 * q + 6] = bf16_lo(u[q].w);
+    v[8 * q + 7] = bf16_hi(u[q].w);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // The kernel. Epi provides:
-//   struct Params; struct State;
+//   struct Params; struct State; struct Pre (registers for a chunk's direct loads);
 //   static constexpr int kChunksPerStore;          // 32-col chunks per store step
+//   static constexpr int kInBoxes;                 // TMA input boxes per chunk (0..2)
+//   __device__ static bool has_input(const Params&, const EpiCtx&, int c);
+//   __device__ static void in_coord(const Params&, const EpiCtx&, int c, int box, int& map, int& x, int& y);
 //   __device__ static int  slots(const Params&);   // TMA store boxes per step (0..2)
 //   __device__ static void begin(State&, const Params&, const EpiCtx&);
+//   __device__ static void prefetch(const Params&, const EpiCtx&, int c, Pre&);  // issue chunk c's loads
 //   __device__ static void chunk(State&, const Params&, const EpiCtx&, int c, float (&acc)[32],
-//                                uint32_t box0, uint32_t box1);
+//                                const Pre&, uint32_t in, uint32_t box0, uint32_t box1);
+//     (`in` = shared address of the chunk's input boxes, 0 if it has none)
 //   __device__ static void store_coord(const Params&, const EpiCtx&, int c, int slot, int& map, int& x, int& y);
 //   __device__ static void end(State&, const Params&, const EpiCtx&);
 // ---------------------------------------------------------------------------
@@ -178,12 +203,15 @@ template <class Epi, int kCG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                         const __grid_constant__ CUtensorMap tmI0, const __grid_constant__ CUtensorMap tmI1,
                          const GemmShape p, const typename Epi::Params ep) {
-  using C = Cfg<kCG>;
+  constexpr int kIn = Epi::kInBoxes;
+  using C = Cfg<kCG, kIn>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_epi + kEpiWarps * kEpiWarpBytes);
+  uint8_t* s_in = s_epi + kEpiWarps * kEpiWarpBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + C::kInBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -201,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
+  auto in_bar = [&](int ew_, int slot) { return smem_u32(bars + 2 * C::kStages + 5 + ew_ * kMaxInSlots + slot); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -212,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(b), kEpiWarps * kCG);
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < kEpiWarps * kMaxInSlots; ++i) mbar_init(in_bar(i / kMaxInSlots, i % kMaxInSlots), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -353,19 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (every CTA)
+    // Chunk c+1's global loads are issued before chunk c is read from TMEM, and
+    // the next tile's first chunk before waiting for that tile's accumulator,
+    // so load latency overlaps TMEM reads, math and the mainloop.
     const int ew = warp & 3;
     const uint32_t my_stage = smem_u32(s_epi) + ew * kEpiWarpBytes;
-    int local = 0;
-    int sbuf = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++local) {
-      const int buf = local & 1;
-      const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
-      if (!wait_bounded(tfull_bar(buf), tphase, p, abort_flag)) break;
-      tc_fence_after();
-      EpiCtx cx;
+    auto make_ctx = [&](int tt, EpiCtx& cx) {
       cx.M = p.M;
       cx.N = p.N;
-      tile_coords(t, p, cx.m_blk, cx.n_blk);
+      tile_coords(tt, p, cx.m_blk, cx.n_blk);
       cx.m0 = cx.m_blk * C::kTileM + static_cast<int>(rank) * BM;
       cx.n0 = cx.n_blk * BN;
       cx.n_blocks = p.n_blocks;
@@ -374,12 +400,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       cx.wrow0 = cx.m0 + 32 * ew;
       cx.row = cx.wrow0 + lane;
       cx.k_blocks = p.k_blocks;
+    };
+    int local = 0;
+    int sbuf = 0;
+    const int nslots = Epi::slots(ep);
+    typename Epi::Pre pa, pb;
+    EpiCtx cx, nx;
+    int t = cluster_id;
+    if (t < p.num_tiles) {
+      make_ctx(t, cx);
+      Epi::prefetch(ep, cx, 0, pa);
+    }
+
+    // Input ring: lane 0 keeps up to kInSlots chunks' input boxes in flight,
+    // running ahead across tile boundaries; every lane consumes them in order.
+    const uint32_t in_base = smem_u32(s_in) + ew * kInWarpBytes;
+    uint32_t seq_used = 0;     // chunks consumed (all lanes)
+    uint32_t seq_issued = 0;   // chunks issued (lane 0)
+    int it_t = t, it_c = 0;    // issue cursor (lane 0)
+    EpiCtx ic = cx;
+    auto issue_ahead = [&]() {
+      if constexpr (kIn > 0) {
+        while (it_t < p.num_tiles && seq_issued < seq_used + C::kInSlots) {
+          if (Epi::has_input(ep, ic, it_c)) {
+            const int slot = static_cast<int>(seq_issued % C::kInSlots);
+            const uint32_t bar = in_bar(ew, slot);
+            const uint32_t dst = in_base + slot * kIn * kInBoxBytes;
+            mbar_arrive_expect_tx(bar, kIn * kInBoxBytes);
+#pragma unroll
+            for (int b = 0; b < kIn; ++b) {
+              int map, x, y;
+              Epi::in_coord(ep, ic, it_c, b, map, x, y);
+              tma_load_2d(dst + b * kInBoxBytes, map ? &tmI1 : &tmI0, bar, x, y);
+            }
+            ++seq_issued;
+          }
+          if (++it_c == BN / 32) {
+            it_c = 0;
+            it_t += num_clusters;
+            if (it_t < p.num_tiles) make_ctx(it_t, ic);
+          }
+        }
+      }
+    };
+    if (lane == 0) issue_ahead();
+    bool ok = true;
+
+    for (; t < p.num_tiles && ok; t += num_clusters, ++local) {
+      const int buf = local & 1;
+      const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
+      if (!wait_bounded(tfull_bar(buf), tphase, p, abort_flag)) break;
+      tc_fence_after();
       typename Epi::State st;
       Epi::begin(st, ep, cx);
-      const int nslots = Epi::slots(ep);
+      const int tn = t + num_clusters;
+      if (tn < p.num_tiles) make_ctx(tn, nx);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      auto do_chunk = [&](int c, const typename Epi::Pre& pre) {
+        uint32_t in = 0;
+        if constexpr (kIn > 0) {
+          if (Epi::has_input(ep, cx, c)) {
+            const int slot = static_cast<int>(seq_used % C::kInSlots);
+            if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
+            in = in_base + slot * kIn * kInBoxBytes;
+          }
+        }
         float acc[32];
         tmem_ld32(tbase + 32 * c, acc);
         if (p.k_blocks == 0) {
@@ -394,7 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
         }
-        Epi::chunk(st, ep, cx, c, acc, box0, box1);
+        Epi::chunk(st, ep, cx, c, acc, pre, in, box0, box1);
+        if constexpr (kIn > 0) {
+          if (in) {
+            // every lane has read the slot: order those reads before the TMA
+            // write that refills it
+            fence_proxy_async_smem();
+            __syncwarp();
+            ++seq_used;
+            if (lane == 0) issue_ahead();
+          }
+        }
         if (nslots > 0 && (c % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1) {
           fence_proxy_async_smem();
           __syncwarp();
@@ -408,6 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sbuf ^= 1;
         }
+      };
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; c += 2) {
+        Epi::prefetch(ep, cx, c + 1, pb);
+        do_chunk(c, pa);
+        if (c + 2 < BN / 32)
+          Epi::prefetch(ep, cx, c + 2, pa);
+        else if (tn < p.num_tiles)
+          Epi::prefetch(ep, nx, 0, pa);
+        do_chunk(c + 1, pb);
       }
       // accumulator buffer fully read: hand it back to the MMA issuer
       tc_fence_before();
@@ -419,8 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(tempty_bar(buf));
       }
       Epi::end(st, ep, cx);
+      cx = nx;
     }
-    if (lane == 0) bulk_wait_all<0>();
+    if (lane == 0) {
+      bulk_wait_all<0>();
+      // input boxes still in flight (only after an abort) land before exit
+      if constexpr (kIn > 0)
+        for (uint32_t q = seq_used; q < seq_issued; ++q)
+          wait_drain(in_bar(ew, static_cast<int>(q % C::kInSlots)), (q / C::kInSlots) & 1u, p.timeout_ns);
+    }
     __syncwarp();
   }
 

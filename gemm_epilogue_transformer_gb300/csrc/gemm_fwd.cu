@@ -48,8 +48,8 @@ int coda_gemm(int M, int N, int K, const coda_bf16* A, int lda, int transA, cons
   EpiPlain::Params ep{0};
   // transA = 1: A stored [K, M] is M-major. transB = 0: B stored [K, N] is
   // N-major; transB = 1: B stored [N, K] is K-major.
-  return launch_fused<EpiPlain>(fn, M, N, K, A, lda, /*a_mn=*/transA, B, ldb, /*b_mn=*/transB ? 0 : 1, o, o, ep,
-                                as_stream(stream));
+  return launch_fused<EpiPlain>(fn, M, N, K, A, lda, /*a_mn=*/transA, B, ldb, /*b_mn=*/transB ? 0 : 1, o, o, o, o,
+                                ep, as_stream(stream));
 }
 
 int coda_gemm_res_rmsprep(int M, int N, int K, const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -67,9 +67,11 @@ int coda_gemm_res_rmsprep(int M, int N, int K, const coda_bf16* x, const coda_bf
   CUtensorMap o0, o1;
   if ((rc = make_out_map(&o0, h1_out, M, N, N))) return rc;
   if ((rc = make_out_map(&o1, h2_out, M, N, N))) return rc;
+  CUtensorMap iz;
+  if ((rc = make_out_map(&iz, z, M, N, N))) return rc;
   EpiResRmsPrep::Params ep{reinterpret_cast<const __nv_bfloat16*>(z), reinterpret_cast<const __nv_bfloat16*>(gamma),
                            psq_out};
-  return launch_fused<EpiResRmsPrep>(fn, M, N, K, x, K, 0, W0, N, /*b_mn=*/1, o0, o1, ep, as_stream(stream));
+  return launch_fused<EpiResRmsPrep>(fn, M, N, K, x, K, 0, W0, N, /*b_mn=*/1, o0, o1, iz, iz, ep, as_stream(stream));
 }
 
 int coda_gemm_rowscale(int M, int N, int K, const coda_bf16* h2, const coda_bf16* W1, const float* r,
@@ -83,7 +85,7 @@ int coda_gemm_rowscale(int M, int N, int K, const coda_bf16* h2, const coda_bf16
   CUtensorMap o;
   if ((rc = make_out_map(&o, Y_out, M, N, N))) return rc;
   EpiRowScale::Params ep{r};
-  return launch_fused<EpiRowScale>(fn, M, N, K, h2, K, 0, W1, N, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  return launch_fused<EpiRowScale>(fn, M, N, K, h2, K, 0, W1, N, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 int coda_gemm_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* Wgu, coda_bf16* A_out,
@@ -100,7 +102,23 @@ int coda_gemm_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* W
   CUtensorMap o;
   if ((rc = make_out_map(&o, A_out, M, F, F))) return rc;
   EpiSwiGLU::Params ep{reinterpret_cast<__nv_bfloat16*>(gu_out)};
-  return launch_fused<EpiSwiGLU>(fn, M, 2 * F, K, X, K, 0, Wgu, 2 * F, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  return launch_fused<EpiSwiGLU>(fn, M, 2 * F, K, X, K, 0, Wgu, 2 * F, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
+}
+
+// TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16
+// frequencies (64 bytes) per box. Used when S % 32 == 0, so that a warp's 32
+// rows never wrap inside a box; otherwise the epilogue loads the tables directly.
+static int rope_table_maps(int tma, const float* c, const float* s, int S, int head_dim, const CUtensorMap& other,
+                           CUtensorMap* tc, CUtensorMap* ts) {
+  if (!tma) {
+    *tc = other;
+    *ts = other;
+    return CODA_OK;
+  }
+  const uint64_t half = static_cast<uint64_t>(head_dim / 2);
+  int rc = make_map_f32(tc, c, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc) return rc;
+  return make_map_f32(ts, s, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 static int rope_common(const char* fn, int M, int N, int K, const coda_bf16* X, const coda_bf16* W,
@@ -124,10 +142,12 @@ int coda_gemm_rope(int M, int N, int K, const coda_bf16* X, const coda_bf16* W, 
   const char* fn = "coda_gemm_rope";
   int rc = rope_common(fn, M, N, K, X, W, cos_tab, sin_tab, S, head_dim, rope_cols, out);
   if (rc || M == 0 || N == 0) return rc;
-  CUtensorMap o;
+  CUtensorMap o, tc, ts;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols};
-  return launch_fused<EpiRope<1>>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  const int tma = S % 32 == 0;
+  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
+  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma};
+  return launch_fused<EpiRope<1>>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, tc, ts, ep, as_stream(stream));
 }
 
 int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16* B, const float* cos_tab,
@@ -136,10 +156,12 @@ int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16*
   const char* fn = "coda_gemm_rope_bwd";
   int rc = rope_common(fn, M, N, K, A, B, cos_tab, sin_tab, S, head_dim, rope_cols, out);
   if (rc || M == 0 || N == 0) return rc;
-  CUtensorMap o;
+  CUtensorMap o, tc, ts;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  EpiRope<-1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols};
-  return launch_fused<EpiRope<-1>>(fn, M, N, K, A, K, 0, B, N, /*b_mn=*/1, o, o, ep, as_stream(stream));
+  const int tma = S % 32 == 0;
+  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
+  EpiRope<-1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma};
+  return launch_fused<EpiRope<-1>>(fn, M, N, K, A, K, 0, B, N, /*b_mn=*/1, o, o, tc, ts, ep, as_stream(stream));
 }
 
 }  // extern "C"

@@ -22,8 +22,9 @@ inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, in
 template <class Epi, int kCG>
 int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, const void* A, int lda, int a_mn,
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
-                   const typename Epi::Params& ep, cudaStream_t stream) {
-  using C = Cfg<kCG>;
+                   const CUtensorMap& i0, const CUtensorMap& i1, const typename Epi::Params& ep,
+                   cudaStream_t stream) {
+  using C = Cfg<kCG, Epi::kInBoxes>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
@@ -83,7 +84,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   }
   const int clusters = p.num_tiles < max_clusters[dev] ? p.num_tiles : max_clusters[dev];
   cfg.gridDim = dim3(clusters * kCG, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, o0, o1, p, ep);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, o0, o1, i0, i1, p, ep);
   if (e != cudaSuccess) return fail_cuda(e, fn);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, fn);
@@ -93,16 +94,18 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
 // One persistent CTA (kCG = 1) or CTA pair (kCG = 2) per SM / SM pair. The
 // pair variant is used once M spans more than one 128-row block, unless
 // coda_set_cta_group() fixed the choice.
+// o0 / o1: TMA store targets; i0 / i1: TMA sources of the epilogue's input
+// boxes (unused maps may be any valid map).
 template <class Epi>
 int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb,
-                 int b_mn, const CUtensorMap& o0, const CUtensorMap& o1, const typename Epi::Params& ep,
-                 cudaStream_t stream) {
+                 int b_mn, const CUtensorMap& o0, const CUtensorMap& o1, const CUtensorMap& i0,
+                 const CUtensorMap& i1, const typename Epi::Params& ep, cudaStream_t stream) {
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int forced = cta_group_setting();
   const int g = forced ? forced : (M > BM ? 2 : 1);
-  if (g == 2) return launch_variant<Epi, 2>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, ep, stream);
-  return launch_variant<Epi, 1>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, ep, stream);
+  if (g == 2) return launch_variant<Epi, 2>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream);
+  return launch_variant<Epi, 1>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream);
 }
 
 }  // namespace coda

@@ -45,5 +45,8 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 // `row_bytes`, box {box_inner, box_outer}, the given swizzle.
 int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+// The same for an fp32 array.
+int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 }  // namespace coda

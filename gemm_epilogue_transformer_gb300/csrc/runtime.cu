@@ -96,15 +96,15 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+static int make_map(CUtensorMapDataType dt, CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(CODA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -112,6 +112,16 @@ int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
                 static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
                 (unsigned long long)row_bytes, box_inner, box_outer);
   return CODA_OK;
+}
+
+int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  return make_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m, base, inner, outer, row_bytes, box_inner, box_outer, sw);
+}
+
+int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  return make_map(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, base, inner, outer, row_bytes, box_inner, box_outer, sw);
 }
 
 }  // namespace coda
