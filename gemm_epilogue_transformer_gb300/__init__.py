@@ -16,7 +16,7 @@ import torch
 from . import _lib
 
 __all__ = [
-    "CodaError", "lib", "coda_init", "coda_device_status", "coda_set_wait_timeout_ns", "coda_set_cta_group",
+    "CodaError", "lib", "coda_init", "coda_device_status", "coda_set_wait_timeout_ns", "coda_set_cta_group", "coda_test_inject_missing_load",
     "coda_num_col_tiles", "coda_num_row_tiles", "coda_gemm", "coda_gemm_res_rmsprep", "coda_rms_reduce",
     "coda_gemm_rowscale", "coda_gemm_swiglu", "coda_gemm_swiglu_bwd", "coda_rope_tables", "coda_gemm_rope",
     "coda_gemm_rope_bwd", "coda_gemm_ce_lse", "coda_ce_reduce", "coda_gemm_ce_bwd", "coda_gemm_rowdot",
@@ -97,6 +97,11 @@ def coda_set_wait_timeout_ns(ns: int):
 def coda_set_cta_group(g: int):
     """0 = automatic, 1 = single-SM 128 x 256 tiles, 2 = SM-pair 256 x 256 tiles."""
     _check(lib().coda_set_cta_group(int(g)))
+
+
+def coda_test_inject_missing_load():
+    """Test hook: the next fused-GEMM launch skips its first stage fill (see coda.h)."""
+    _check(lib().coda_test_inject_missing_load())
 
 
 def coda_num_col_tiles(N: int) -> int:

@@ -80,6 +80,7 @@ struct EpiPlain {
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&, uint32_t,
@@ -110,6 +111,7 @@ struct EpiResRmsPrep {
   }
   CODA_INPUT_SAME_TILE  // z
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params&, const EpiCtx&) { st.sumsq = 0.f; }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre& pr,
@@ -147,6 +149,7 @@ struct EpiRowScale {
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
@@ -165,28 +168,25 @@ struct EpiRowScale {
 // Even column = gate G, odd = up U; out[f] = silu(G) * U; the 32 accumulator
 // columns of a chunk give 16 outputs, two chunks fill one 32-column store box
 // (CODA note, Key design 2: halve the width and compact before the store).
-// Optional side output: the pre-activation GU itself (bf16), for the backward.
+// kSaveGU: also store the pre-activation GU (bf16) for the backward, one more
+// store box per chunk (a separate instantiation: the extra staging box costs
+// one mainloop stage, which the plain forward keeps).
+template <bool kSaveGU>
 struct EpiSwiGLU {
   struct Params {
-    __nv_bfloat16* gu;  // nullable, [M, 2F]
+    int unused;
   };
   struct State {};
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 2;
-  __device__ static int slots(const Params&) { return 1; }
+  static constexpr int kMaxSlots = kSaveGU ? 3 : 2;
+  // slot 0: A (32 outputs from two chunks); slots 1, 2: GU of the two chunks
+  __device__ static int slots(const Params&) { return kSaveGU ? 3 : 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
+  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
                                uint32_t, uint32_t box0, uint32_t) {
-    const int col0 = cx.n0 + 32 * c;
-    if (ep.gu != nullptr && cx.row < cx.M) {
-      uint4* dst = reinterpret_cast<uint4*>(ep.gu + static_cast<long>(cx.row) * cx.N + col0);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (col0 + 8 * q < cx.N)
-          dst[q] = make_uint4(pack_bf16(acc[8 * q + 0], acc[8 * q + 1]), pack_bf16(acc[8 * q + 2], acc[8 * q + 3]),
-                              pack_bf16(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16(acc[8 * q + 6], acc[8 * q + 7]));
-    }
+    if (kSaveGU) stage_row32(box0 + (1 + (c & 1)) * kStageBoxBytes, cx.lane, acc);
     float o[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -199,10 +199,15 @@ struct EpiSwiGLU {
     stage_put(box0, cx.lane, h + 1, pack_bf16(o[8], o[9]), pack_bf16(o[10], o[11]), pack_bf16(o[12], o[13]),
               pack_bf16(o[14], o[15]));
   }
-  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
-    map = 0;
-    x = cx.n0 / 2 + 16 * (c - 1);
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
     y = cx.wrow0;
+    if (s == 0) {
+      map = 0;
+      x = cx.n0 / 2 + 16 * (c - 1);
+    } else {
+      map = 1;
+      x = cx.n0 + 32 * (c - 2 + s);
+    }
   }
   __device__ static void end(State&, const Params&, const EpiCtx&) {}
 };
@@ -226,6 +231,7 @@ struct EpiSwiGLUBwd {
     y = cx.wrow0;
   }
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
@@ -298,6 +304,7 @@ struct EpiRope {
     }
   }
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
@@ -364,6 +371,7 @@ struct EpiCeLse {
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 0; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.m = -INFINITY;
@@ -439,6 +447,7 @@ struct EpiCeBwd {
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.label = (cx.row < cx.M) ? ep.labels[cx.row] : -1;
@@ -475,6 +484,7 @@ struct EpiRowdot {
   CODA_NO_PREFETCH
   CODA_INPUT_SAME_TILE  // Y
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params& ep) { return ep.store_dyr ? 2 : 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = 0.f;
@@ -523,6 +533,7 @@ struct EpiRmsNormBwd {
   }
   CODA_INPUT_SAME_TILE  // h1
   static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     if (cx.row < cx.M) {

@@ -40,9 +40,7 @@ constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
 constexpr int kStageBoxBytes = 32 * 64;  // one epilogue TMA store box: 32 rows x 64 bytes
-constexpr int kEpiSlots = 2;             // store boxes per staging buffer
 constexpr int kEpiBufs = 2;              // staging double buffer
-constexpr int kEpiWarpBytes = kStageBoxBytes * kEpiSlots * kEpiBufs;
 // Rank-2 epilogue inputs (z, Y, h1, GU, RoPE tables) arrive by TMA in 32 x 64B
 // boxes into a per-warp ring of kInWarpBytes, issued several chunks ahead.
 constexpr int kInBoxBytes = 32 * 64;
@@ -55,14 +53,18 @@ constexpr int kMaxInSlots = 4;
 // of 48 KiB and the ring is 6 deep instead of 4. kIn = input boxes per chunk
 // (0, 1, 2): epilogues with inputs give one mainloop stage to the input ring
 // (a 5-deep ring measured as fast as a 6-deep one for the pair variant).
-template <int kCG, int kIn>
+// kSlots = store boxes per staging buffer (2, or 3 for SwiGLU with its
+// pre-activation side output, which also takes the shorter ring).
+template <int kCG, int kIn, int kSlots>
 struct Cfg {
   static constexpr int kTileM = BM * kCG;
   static constexpr int kBLoad = BN / kCG;  // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = kBLoad * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kCG == 1 ? (kIn ? 3 : 4) : (kIn ? 5 : 6);
+  static constexpr int kEpiWarpBytes = kStageBoxBytes * kSlots * kEpiBufs;
+  static constexpr bool kShortRing = kIn > 0 || kSlots > 2;
+  static constexpr int kStages = kCG == 1 ? (kShortRing ? 3 : 4) : (kShortRing ? 5 : 6);
   static constexpr int kInSlots = kIn ? kInWarpBytes / (kIn * kInBoxBytes) : 0;
   static constexpr int kInBytes = kIn ? kEpiWarps * kInWarpBytes : 0;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
@@ -70,19 +72,31 @@ struct Cfg {
       1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kInSlots <= kMaxInSlots, "input ring slots");
+  static_assert(kSlots == 2 || kSlots == 3, "staging slots");
 };
+
+constexpr int BSEG = 128;  // epilogue segment: columns per partial-statistics block
 
 struct GemmShape {
   int M, N, K;
   int a_mn, b_mn;
   int m_blocks, n_blocks, k_blocks, num_tiles, group_m;
+  // Work items: the first full_items are whole tiles in raster order; each of
+  // the remaining tiles (a partial last wave) is split into two 128-column
+  // halves so the last wave takes half a tile's time. num_items in total.
+  int full_items, num_items;
+  int seg_blocks;  // ceil(N / 128): second dimension of the [M, seg_blocks] partials
   int* status;                    // device status word (CODA_DEVST_* bits)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
+  int inject;                     // test hook: 1 = producers skip their first stage fill
 };
 
 struct EpiCtx {
   int M, N;
-  int m0, n0, m_blk, n_blk, n_blocks;
+  int m0, n0;   // this segment's first row (of the CTA's 128) and first column
+  int m_blk;
+  int n_blk;    // n0 / 128: the column block of the segment's partial statistics
+  int n_blocks; // ceil(N / 128)
   int row;    // this thread's accumulator row (global index)
   int wrow0;  // first row of this warp's 32-row slice (global index)
   int ew;     // warp quarter (TMEM lanes 32*ew .. 32*ew+31)
@@ -92,6 +106,21 @@ struct EpiCtx {
 
 // Tile order: groups of group_m row-blocks sweep all column blocks, so the
 // A rows of a group and the B columns in flight stay L2 resident.
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_blk, int& n_blk);
+// Work item t -> row block, first column and width (256 or 128 columns).
+__device__ __forceinline__ void item_coords(int t, const GemmShape& p, int& m_blk, int& n0, int& ncols) {
+  int n_blk;
+  if (t < p.full_items) {
+    tile_coords(t, p, m_blk, n_blk);
+    n0 = n_blk * BN;
+    ncols = BN;
+  } else {
+    const int h = t - p.full_items;
+    tile_coords(p.full_items + (h >> 1), p, m_blk, n_blk);
+    n0 = n_blk * BN + (h & 1) * BSEG;
+    ncols = BSEG;
+  }
+}
 __device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_blk, int& n_blk) {
   const int per_group = p.group_m * p.n_blocks;
   const int g = t / per_group;
@@ -125,6 +154,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
                                              volatile int* abort_flag) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   return wait_bounded_slow(bar, parity, p, abort_flag);
+}
+// Bounded wait for long waits off the critical path (the epilogue waiting for
+// the next accumulator): the thread sleeps on the barrier between checks, so
+// it does not take issue slots from the producer and MMA threads that share
+// its SM sub-partition.
+static __device__ __noinline__ bool wait_bounded_sleep(uint32_t bar, uint32_t parity, const GemmShape& p,
+                                                       volatile int* abort_flag) {
+  if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      atomicOr(p.status, CODA_DEVST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
 }
 // Bounded wait used while draining after an abort: ignores the abort flag.
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
@@ -188,9 +235,10 @@ __device__ __forceinline__ void unpack32(const uint4 (&u)[4], float (&v)[32]) {
 //   struct Params; struct State; struct Pre (registers for a chunk's direct loads);
 //   static constexpr int kChunksPerStore;          // 32-col chunks per store step
 //   static constexpr int kInBoxes;                 // TMA input boxes per chunk (0..2)
+//   static constexpr int kMaxSlots;                // staging boxes per store step (2 or 3)
 //   __device__ static bool has_input(const Params&, const EpiCtx&, int c);
 //   __device__ static void in_coord(const Params&, const EpiCtx&, int c, int box, int& map, int& x, int& y);
-//   __device__ static int  slots(const Params&);   // TMA store boxes per step (0..2)
+//   __device__ static int  slots(const Params&);   // TMA store boxes per step (0..kMaxSlots)
 //   __device__ static void begin(State&, const Params&, const EpiCtx&);
 //   __device__ static void prefetch(const Params&, const EpiCtx&, int c, Pre&);  // issue chunk c's loads
 //   __device__ static void chunk(State&, const Params&, const EpiCtx&, int c, float (&acc)[32],
@@ -206,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmI0, const __grid_constant__ CUtensorMap tmI1,
                          const GemmShape p, const typename Epi::Params ep) {
   constexpr int kIn = Epi::kInBoxes;
-  using C = Cfg<kCG, kIn>;
+  constexpr int kSlots = Epi::kMaxSlots;
+  using C = Cfg<kCG, kIn, kSlots>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
-  uint8_t* s_in = s_epi + kEpiWarps * kEpiWarpBytes;
+  uint8_t* s_in = s_epi + kEpiWarps * C::kEpiWarpBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + C::kInBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -269,22 +318,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fills[C::kStages];
-#pragma unroll
-      for (int s = 0; s < C::kStages; ++s) fills[s] = 0;
+      uint32_t issued = 0;  // stage fills issued (for the drain)
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
-        int m_blk, n_blk;
-        tile_coords(t, p, m_blk, n_blk);
+      if (p.inject == 1) {
+        // test hook: the first fill is never issued, so the MMA's wait on it
+        // must run out and take the abort path (the outputs are then undefined)
+        stage = 1;
+        issued = 1;
+      }
+      for (int t = cluster_id; t < p.num_items && ok; t += num_clusters) {
+        int m_blk, n0, ncols;
+        item_coords(t, p, m_blk, n0, ncols);
         const int m0 = m_blk * C::kTileM + static_cast<int>(rank) * BM;
-        const int nb0 = n_blk * BN + static_cast<int>(rank) * C::kBLoad;
+        const int bcols = ncols / kCG;  // B columns this CTA loads
+        const int nb0 = n0 + static_cast<int>(rank) * bcols;
+        // N-major B arrives in 64-column boxes; K-major B as one box of
+        // kBLoad rows (a half tile reads past its columns: harmless extra bytes)
+        const int nbox = p.b_mn ? bcols / 64 : 0;
+        const uint32_t tx = kCG * (C::kABytes + (p.b_mn ? static_cast<uint32_t>(bcols * BK * 2) : C::kBBytes));
+        // The k-loop is the kernel's critical path: keep it to the wait, the
+        // expected-bytes arrive and the copies.
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
-          if (leader) mbar_arrive_expect_tx(fb, kCG * C::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(fb, tx);
           const uint32_t fb_target = kCG == 2 ? mapa_shared(fb, 0) : fb;
           const uint32_t a_dst = s_base + stage * C::kStageBytes;
           const uint32_t b_dst = a_dst + C::kABytes;
@@ -303,11 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (p.b_mn) {
 #pragma unroll
-            for (int j = 0; j < C::kBLoad / 64; ++j) load(b_dst + j * 8192, &tmB, nb0 + 64 * j, k0);
+            for (int j = 0; j < C::kBLoad / 64; ++j)
+              if (j < nbox) load(b_dst + j * 8192, &tmB, nb0 + 64 * j, k0);
           } else {
             load(b_dst, &tmB, k0, nb0);
           }
-          fills[stage]++;
+          ++issued;
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -315,16 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Drain: every load signalled on this CTA's full barriers has landed
-      // before the CTA exits (in a pair, all loads signal the leader's).
+      // before the CTA exits (in a pair, all loads signal the leader's). Fill
+      // f of stage s completes phase (f / kStages) & 1 of that stage's barrier.
       if (leader)
-        for (int s = 0; s < C::kStages; ++s)
-          if (fills[s] > 0) wait_drain(full_bar(s), static_cast<uint32_t>((fills[s] - 1) & 1), p.timeout_ns);
+        for (int s = 0; s < C::kStages; ++s) {
+          const uint32_t fills = issued / C::kStages + (static_cast<uint32_t>(s) < issued % C::kStages ? 1u : 0u);
+          if (fills > 0 && !(p.inject == 1 && s == 0 && fills == 1))
+            wait_drain(full_bar(s), (fills - 1) & 1u, p.timeout_ns);
+        }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(C::kTileM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc_full = idesc_bf16_f32(C::kTileM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc_half = idesc_bf16_f32(C::kTileM, BSEG, p.a_mn, p.b_mn);
       // Operand descriptors. K-major: 128B rows, 8-row groups 1024B apart,
       // K advances 32B (16 bf16) inside the swizzle atom. MN-major: 64-element
       // MN chunks 8192B apart (LBO), 8-row K groups 1024B apart (SBO), K
@@ -335,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++local) {
+      for (int t = cluster_id; t < p.num_items && ok; t += num_clusters, ++local) {
+        const uint32_t idesc = t < p.full_items ? idesc_full : idesc_half;
         const int buf = local & 1;
         const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
         if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, p, abort_flag)) break;
@@ -387,42 +454,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the next tile's first chunk before waiting for that tile's accumulator,
     // so load latency overlaps TMEM reads, math and the mainloop.
     const int ew = warp & 3;
-    const uint32_t my_stage = smem_u32(s_epi) + ew * kEpiWarpBytes;
-    auto make_ctx = [&](int tt, EpiCtx& cx) {
+    const uint32_t my_stage = smem_u32(s_epi) + ew * C::kEpiWarpBytes;
+    // Segment `seg` (128 columns) of work item tt; false if it lies past N.
+    auto make_ctx = [&](int tt, int seg, EpiCtx& cx) {
+      int n0, ncols;
+      item_coords(tt, p, cx.m_blk, n0, ncols);
       cx.M = p.M;
       cx.N = p.N;
-      tile_coords(tt, p, cx.m_blk, cx.n_blk);
       cx.m0 = cx.m_blk * C::kTileM + static_cast<int>(rank) * BM;
-      cx.n0 = cx.n_blk * BN;
-      cx.n_blocks = p.n_blocks;
+      cx.n0 = n0 + seg * BSEG;
+      cx.n_blk = cx.n0 / BSEG;
+      cx.n_blocks = p.seg_blocks;
       cx.ew = ew;
       cx.lane = lane;
       cx.wrow0 = cx.m0 + 32 * ew;
       cx.row = cx.wrow0 + lane;
       cx.k_blocks = p.k_blocks;
+      return cx.n0 < p.N;
     };
+    auto item_segs = [&](int tt) { return tt < p.full_items ? BN / BSEG : 1; };
+    constexpr int kSegChunks = BSEG / 32;
     int local = 0;
     int sbuf = 0;
     const int nslots = Epi::slots(ep);
-    typename Epi::Pre pa, pb;
-    EpiCtx cx, nx;
-    int t = cluster_id;
-    if (t < p.num_tiles) {
-      make_ctx(t, cx);
-      Epi::prefetch(ep, cx, 0, pa);
-    }
 
     // Input ring: lane 0 keeps up to kInSlots chunks' input boxes in flight,
-    // running ahead across tile boundaries; every lane consumes them in order.
+    // running ahead across segments and work items; every lane consumes them
+    // in the same order.
     const uint32_t in_base = smem_u32(s_in) + ew * kInWarpBytes;
-    uint32_t seq_used = 0;     // chunks consumed (all lanes)
-    uint32_t seq_issued = 0;   // chunks issued (lane 0)
-    int it_t = t, it_c = 0;    // issue cursor (lane 0)
-    EpiCtx ic = cx;
+    uint32_t seq_used = 0;    // chunks consumed (all lanes)
+    uint32_t seq_issued = 0;  // chunks issued (lane 0)
+    int it_t = cluster_id, it_s = 0, it_c = 0;  // issue cursor (lane 0)
+    EpiCtx ic;
+    bool ic_ok = it_t < p.num_items && make_ctx(it_t, 0, ic);
     auto issue_ahead = [&]() {
       if constexpr (kIn > 0) {
-        while (it_t < p.num_tiles && seq_issued < seq_used + C::kInSlots) {
-          if (Epi::has_input(ep, ic, it_c)) {
+        while (it_t < p.num_items && seq_issued < seq_used + C::kInSlots) {
+          if (ic_ok && Epi::has_input(ep, ic, it_c)) {
             const int slot = static_cast<int>(seq_issued % C::kInSlots);
             const uint32_t bar = in_bar(ew, slot);
             const uint32_t dst = in_base + slot * kIn * kInBoxBytes;
@@ -435,84 +503,101 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++seq_issued;
           }
-          if (++it_c == BN / 32) {
+          if (!ic_ok || ++it_c == kSegChunks) {
             it_c = 0;
-            it_t += num_clusters;
-            if (it_t < p.num_tiles) make_ctx(it_t, ic);
+            if (++it_s == item_segs(it_t)) {
+              it_s = 0;
+              it_t += num_clusters;
+            }
+            ic_ok = it_t < p.num_items && make_ctx(it_t, it_s, ic);
           }
         }
       }
     };
     if (lane == 0) issue_ahead();
     bool ok = true;
+    typename Epi::Pre pa, pb;
+    EpiCtx cx;
 
-    for (; t < p.num_tiles && ok; t += num_clusters, ++local) {
+    for (int t = cluster_id; t < p.num_items && ok; t += num_clusters, ++local) {
       const int buf = local & 1;
       const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
-      if (!wait_bounded(tfull_bar(buf), tphase, p, abort_flag)) break;
+      if (!wait_bounded_sleep(tfull_bar(buf), tphase, p, abort_flag)) break;
       tc_fence_after();
-      typename Epi::State st;
-      Epi::begin(st, ep, cx);
-      const int tn = t + num_clusters;
-      if (tn < p.num_tiles) make_ctx(tn, nx);
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
-      auto do_chunk = [&](int c, const typename Epi::Pre& pre) {
-        uint32_t in = 0;
-        if constexpr (kIn > 0) {
-          if (Epi::has_input(ep, cx, c)) {
-            const int slot = static_cast<int>(seq_used % C::kInSlots);
-            if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
-            in = in_base + slot * kIn * kInBoxBytes;
+      // One loop over the item's 8 (or 4) chunks; partial statistics close and
+      // reopen at the 128-column segment boundary (chunk 4). A segment that
+      // starts past N ends the item (only the last column block can).
+      const int nchunks = item_segs(t) * kSegChunks;
+      if (make_ctx(t, 0, cx)) {
+        typename Epi::State st;
+        Epi::begin(st, ep, cx);
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
+        auto do_chunk = [&](int c, const typename Epi::Pre& pre) {
+          const int cs = c & (kSegChunks - 1);  // chunk index inside its segment
+          uint32_t in = 0;
+          if constexpr (kIn > 0) {
+            if (Epi::has_input(ep, cx, cs)) {
+              const int slot = static_cast<int>(seq_used % C::kInSlots);
+              if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
+              in = in_base + slot * kIn * kInBoxBytes;
+            }
           }
-        }
-        float acc[32];
-        tmem_ld32(tbase + 32 * c, acc);
-        if (p.k_blocks == 0) {
+          float acc[32];
+          tmem_ld32(tbase + 32 * c, acc);
+          if (p.k_blocks == 0) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-        }
-        const uint32_t box0 = my_stage + (sbuf * kEpiSlots + 0) * kStageBoxBytes;
-        const uint32_t box1 = box0 + kStageBoxBytes;
-        if (nslots > 0 && (c % Epi::kChunksPerStore) == 0) {
-          // the staging buffer about to be written was last read by the store
-          // group before the most recent one
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-        }
-        Epi::chunk(st, ep, cx, c, acc, pre, in, box0, box1);
-        if constexpr (kIn > 0) {
-          if (in) {
-            // every lane has read the slot: order those reads before the TMA
-            // write that refills it
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+          }
+          // this store step's boxes are contiguous: box k at box0 + k * kStageBoxBytes
+          const uint32_t box0 = my_stage + (sbuf * kSlots) * kStageBoxBytes;
+          const uint32_t box1 = box0 + kStageBoxBytes;
+          if (nslots > 0 && (cs % Epi::kChunksPerStore) == 0) {
+            // the staging buffer about to be written was last read by the store
+            // group before the most recent one
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          Epi::chunk(st, ep, cx, cs, acc, pre, in, box0, box1);
+          if constexpr (kIn > 0) {
+            if (in) {
+              // every lane has read the slot: order those reads before the TMA
+              // write that refills it
+              fence_proxy_async_smem();
+              __syncwarp();
+              ++seq_used;
+              if (lane == 0) issue_ahead();
+            }
+          }
+          if (nslots > 0 && (cs % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1) {
             fence_proxy_async_smem();
             __syncwarp();
-            ++seq_used;
-            if (lane == 0) issue_ahead();
-          }
-        }
-        if (nslots > 0 && (c % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            for (int s = 0; s < nslots; ++s) {
-              int map, x, y;
-              Epi::store_coord(ep, cx, c, s, map, x, y);
-              tma_store_2d(map ? &tmO1 : &tmO0, s == 0 ? box0 : box1, x, y);
+            if (lane == 0) {
+              for (int s = 0; s < nslots; ++s) {
+                int map, x, y;
+                Epi::store_coord(ep, cx, cs, s, map, x, y);
+                tma_store_2d(map ? &tmO1 : &tmO0, box0 + s * kStageBoxBytes, x, y);
+              }
+              bulk_commit();
             }
-            bulk_commit();
+            sbuf ^= 1;
           }
-          sbuf ^= 1;
-        }
-      };
+        };
+        // vector operands: chunk c+1's loads are issued before chunk c runs
+        Epi::prefetch(ep, cx, 0, pa);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; c += 2) {
-        Epi::prefetch(ep, cx, c + 1, pb);
-        do_chunk(c, pa);
-        if (c + 2 < BN / 32)
-          Epi::prefetch(ep, cx, c + 2, pa);
-        else if (tn < p.num_tiles)
-          Epi::prefetch(ep, nx, 0, pa);
-        do_chunk(c + 1, pb);
+        for (int c = 0; c < nchunks; c += 2) {
+          if (c == kSegChunks) {
+            Epi::end(st, ep, cx);
+            if (!make_ctx(t, 1, cx)) break;
+            Epi::begin(st, ep, cx);
+            Epi::prefetch(ep, cx, 0, pa);
+          }
+          Epi::prefetch(ep, cx, (c + 1) & (kSegChunks - 1), pb);
+          do_chunk(c, pa);
+          if (((c + 2) & (kSegChunks - 1)) != 0) Epi::prefetch(ep, cx, (c + 2) & (kSegChunks - 1), pa);
+          do_chunk(c + 1, pb);
+          if (c + 2 == nchunks) Epi::end(st, ep, cx);
+        }
       }
       // accumulator buffer fully read: hand it back to the MMA issuer
       tc_fence_before();
@@ -523,8 +608,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mbar_arrive(tempty_bar(buf));
       }
-      Epi::end(st, ep, cx);
-      cx = nx;
     }
     if (lane == 0) {
       bulk_wait_all<0>();

@@ -99,10 +99,18 @@ int coda_gemm_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* W
   if (M == 0 || F == 0) return CODA_OK;
   CODA_REQ_PTR16(A_out);
   CODA_REQ_OPT16(gu_out);
-  CUtensorMap o;
+  CUtensorMap o, og;
   if ((rc = make_out_map(&o, A_out, M, F, F))) return rc;
-  EpiSwiGLU::Params ep{reinterpret_cast<__nv_bfloat16*>(gu_out)};
-  return launch_fused<EpiSwiGLU>(fn, M, 2 * F, K, X, K, 0, Wgu, 2 * F, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
+  og = o;
+  if (gu_out && (rc = make_out_map(&og, gu_out, M, 2 * F, 2 * F))) return rc;
+  if (gu_out) {
+    EpiSwiGLU<true>::Params ep{0};
+    return launch_fused<EpiSwiGLU<true>>(fn, M, 2 * F, K, X, K, 0, Wgu, 2 * F, /*b_mn=*/1, o, og, o, o, ep,
+                                         as_stream(stream));
+  }
+  EpiSwiGLU<false>::Params ep{0};
+  return launch_fused<EpiSwiGLU<false>>(fn, M, 2 * F, K, X, K, 0, Wgu, 2 * F, /*b_mn=*/1, o, og, o, o, ep,
+                                        as_stream(stream));
 }
 
 // TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16

@@ -24,7 +24,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
                    const CUtensorMap& i0, const CUtensorMap& i1, const typename Epi::Params& ep,
                    cudaStream_t stream) {
-  using C = Cfg<kCG, Epi::kInBoxes>;
+  using C = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
@@ -38,20 +38,6 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
-  GemmShape p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.a_mn = a_mn;
-  p.b_mn = b_mn;
-  p.m_blocks = (M + C::kTileM - 1) / C::kTileM;
-  p.n_blocks = (N + BN - 1) / BN;
-  p.k_blocks = (K + BK - 1) / BK;
-  p.num_tiles = p.m_blocks * p.n_blocks;
-  p.group_m = p.m_blocks < kGroupM / kCG ? p.m_blocks : kGroupM / kCG;
-  p.status = di->status;
-  p.timeout_ns = wait_timeout_ns();
-
   auto kernel = &gemm_epilogue_kernel<Epi, kCG>;
   static int max_clusters[64] = {0};  // per device; 0 = not yet queried
   int dev = 0;
@@ -82,7 +68,35 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
     }
     max_clusters[dev] = n;
   }
-  const int clusters = p.num_tiles < max_clusters[dev] ? p.num_tiles : max_clusters[dev];
+  const int cmax = max_clusters[dev];
+
+  GemmShape p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.m_blocks = (M + C::kTileM - 1) / C::kTileM;
+  p.n_blocks = (N + BN - 1) / BN;
+  p.k_blocks = (K + BK - 1) / BK;
+  p.num_tiles = p.m_blocks * p.n_blocks;
+  p.group_m = p.m_blocks < kGroupM / kCG ? p.m_blocks : kGroupM / kCG;
+  p.seg_blocks = (N + BSEG - 1) / BSEG;
+  // Wave balance: a last wave of `rem` tiles that fills at most half of the
+  // persistent clusters runs as 2 * rem half tiles (256 x 128) instead.
+  const int rem = p.num_tiles % cmax;
+  if (rem > 0 && 2 * rem <= cmax && N > BSEG) {
+    p.full_items = p.num_tiles - rem;
+    p.num_items = p.num_tiles + rem;
+  } else {
+    p.full_items = p.num_tiles;
+    p.num_items = p.num_tiles;
+  }
+  p.status = di->status;
+  p.timeout_ns = wait_timeout_ns();
+  p.inject = take_injected_fault();
+
+  const int clusters = p.num_items < cmax ? p.num_items : cmax;
   cfg.gridDim = dim3(clusters * kCG, 1, 1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, o0, o1, i0, i1, p, ep);
   if (e != cudaSuccess) return fail_cuda(e, fn);

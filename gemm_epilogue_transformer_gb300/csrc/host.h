@@ -25,6 +25,8 @@ const DeviceInfo* current_device();
 unsigned long long wait_timeout_ns();
 // 0 = choose per launch, 1 = single-SM tiles, 2 = SM-pair tiles (coda_set_cta_group).
 int cta_group_setting();
+// Consume the one-shot test fault set by coda_test_inject_missing_load().
+int take_injected_fault();
 
 // ---------------------------------------------------------------- checks
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

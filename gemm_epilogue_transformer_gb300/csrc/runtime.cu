@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "host.h"
@@ -14,6 +15,7 @@ namespace coda {
 static thread_local char g_err[1024] = "";
 static unsigned long long g_timeout_ns = 2000000000ull;
 static int g_cta_group = 0;
+static std::atomic<int> g_inject{0};
 
 // The device status word (CODA_DEVST_* bits). Kernels receive its device
 // address, obtained per device with cudaGetSymbolAddress.
@@ -77,6 +79,7 @@ const DeviceInfo* current_device() {
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 int cta_group_setting() { return g_cta_group; }
+int take_injected_fault() { return g_inject.exchange(0); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -166,7 +169,12 @@ int coda_set_cta_group(int g) {
   return CODA_OK;
 }
 
-int coda_num_col_tiles(int N) { return N <= 0 ? 0 : (N + 255) / 256; }
+int coda_test_inject_missing_load(void) {
+  g_inject.store(1);
+  return CODA_OK;
+}
+
+int coda_num_col_tiles(int N) { return N <= 0 ? 0 : (N + 127) / 128; }
 int coda_num_row_tiles(int M) { return M <= 0 ? 0 : (M + 31) / 32; }
 
 }  // extern "C"

@@ -81,8 +81,16 @@ int coda_set_wait_timeout_ns(unsigned long long ns);
  * rejected with CODA_ERR_INVALID. */
 int coda_set_cta_group(int g);
 
-/* Number of column tiles of a fused kernel's output for GEMM width N
- * (ceil(N / 256)): the second dimension of every [M, nb] partial buffer. */
+/* Test hook for the failure-detection path: the next fused-GEMM launch from
+ * this process skips the producers' first stage fill, so the MMA issuer's
+ * bounded wait on it runs out. The kernel then sets CODA_DEVST_TIMEOUT, stops
+ * every role, drains the copies and MMAs it issued, frees TMEM and returns;
+ * its outputs are undefined. Use with a short coda_set_wait_timeout_ns(). */
+int coda_test_inject_missing_load(void);
+
+/* Number of 128-column blocks of a fused kernel's output for GEMM width N
+ * (ceil(N / 128)): the second dimension of every [M, nb] partial buffer.
+ * Each partial covers one 128-column block of one row. */
 int coda_num_col_tiles(int N);
 
 /* Number of row tiles used by the column partials of coda_gemm_rmsnorm_bwd
@@ -104,7 +112,7 @@ int coda_gemm(int M, int N, int K, const coda_bf16* A, int lda, int transA, cons
  * with r the per-row inverse RMS, applied in the second GEMM's epilogue.
  *
  * coda_gemm_res_rmsprep: first GEMM, epilogue h1 = x W0 + z, h2 = h1 (.) gamma,
- *   psq[i, t] = sum over the columns of tile t of h1[i,j]^2 (fp32 h1, before
+ *   psq[i, t] = sum over the columns of block t of h1[i,j]^2 (fp32 h1, before
  *   rounding; the pages' tile partial of the unscaled residual).
  *   x [M,K], W0 [K,N], z [M,N], gamma [N] -> h1, h2 [M,N] bf16,
  *   psq [M, coda_num_col_tiles(N)] fp32. N, K multiples of 8. */
@@ -167,9 +175,9 @@ int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16*
  * tiles, combined by an auxiliary reduction). Logits L = H W are fp32 in the
  * accumulator and are never stored.
  *
- * coda_gemm_ce_lse: per (row i, column tile t): pmax[i,t] = max_j L[i,j],
+ * coda_gemm_ce_lse: per (row i, 128-column block t): pmax[i,t] = max_j L[i,j],
  *   psum[i,t] = sum_j exp(L[i,j] - pmax[i,t]), parg[i,t] = lowest j attaining
- *   the max (NULL to skip); the tile that holds label y_i writes
+ *   the max (NULL to skip); the block that holds label y_i writes
  *   tgt[i] = L[i, y_i]. H [M,K], W [K,V], labels [M] int32 in [0,V) ->
  *   pmax, psum [M, coda_num_col_tiles(V)] fp32, parg same shape int32, tgt [M].
  *   A label outside [0, V) sets CODA_DEVST_BAD_LABEL and tgt[i] = NaN. */
@@ -197,7 +205,7 @@ int coda_gemm_ce_bwd(int M, int V, int K, const coda_bf16* H, const coda_bf16* W
  *
  * coda_gemm_rowdot: dY = dO Wn; stores dY (bf16), optionally dYr = r (.)row dY
  *   (bf16; NULL to skip, r may then be NULL), and pdot[i,t] = sum over the
- *   columns of tile t of dY[i,j] Y[i,j] (fp32 dY times the stored bf16 Y).
+ *   columns of block t of dY[i,j] Y[i,j] (fp32 dY times the stored bf16 Y).
  *   dO [M,K], Wn [K,N], Y [M,N] -> dY, dYr [M,N], pdot [M, coda_num_col_tiles(N)]. */
 int coda_gemm_rowdot(int M, int N, int K, const coda_bf16* dO, const coda_bf16* Wn, const coda_bf16* Y,
                      const float* r, coda_bf16* dY_out, coda_bf16* dYr_out, float* pdot_out, coda_stream_t stream);

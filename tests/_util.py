@@ -71,7 +71,7 @@ def assert_stat(got, ref, name="", tol=STAT_REL):
     return err
 
 
-def col_tile_sums(x: np.ndarray, tile: int = 256) -> np.ndarray:
-    """Per-(row, column tile) sums: the reference for tile partials."""
+def col_tile_sums(x: np.ndarray, tile: int = 128) -> np.ndarray:
+    """Per-(row, 128-column block) sums: the reference for the epilogue partials."""
     n = x.shape[1]
     return np.stack([x[:, c:c + tile].sum(axis=1) for c in range(0, n, tile)], axis=1) if n else np.zeros((x.shape[0], 0))

@@ -89,7 +89,7 @@ def test_host_validation_rejects_before_launch(lib):
 
 
 def test_tile_counts(lib):
-    assert [lib.coda_num_col_tiles(n) for n in (0, 1, 256, 257, 32768)] == [0, 1, 1, 2, 128]
+    assert [lib.coda_num_col_tiles(n) for n in (0, 1, 128, 129, 32768)] == [0, 1, 1, 2, 256]
     assert [lib.coda_num_row_tiles(m) for m in (0, 1, 32, 33, 8192)] == [0, 1, 1, 2, 256]
 
 

@@ -184,7 +184,7 @@ def test_ce_fwd_bwd(coda, M, K, V):
     L = O.matmul(O.bf16(p["H"]), O.bf16(p["W"]))
     ref = O.ce_fwd(L, p["labels"])
     nb = coda.coda_num_col_tiles(V)
-    tiles = [(t * 256, min(V, t * 256 + 256)) for t in range(nb)]
+    tiles = [(t * 128, min(V, t * 128 + 128)) for t in range(nb)]
     ref_pmax = np.stack([L[:, a:b].max(axis=1) for a, b in tiles], axis=1)
     assert_stat(f64(pmax), ref_pmax, "pmax")
     ref_psum = np.stack([np.exp(L[:, a:b] - f64(pmax)[:, [t]]).sum(axis=1) for t, (a, b) in enumerate(tiles)], axis=1)
