@@ -184,6 +184,15 @@ def ncu_traffic(kernel):
     return d.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (the slowest replica sets the
+    job's time); every rank receives the result."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def main():
     a = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -308,9 +317,7 @@ def main():
     d2h = (M * N + M * K + K * N) * 2
 
     if dist:
-        t = torch.tensor([ms_fused, ms_unfused, ms_e2e, ms_rope], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_fused, ms_unfused, ms_e2e, ms_rope = (float(v) for v in t.tolist())
+        ms_fused, ms_unfused, ms_e2e, ms_rope = max_over_ranks([ms_fused, ms_unfused, ms_e2e, ms_rope], dist, dev)
 
     if rank != 0:
         if dist:
