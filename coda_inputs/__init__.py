@@ -31,6 +31,8 @@ __all__ = [
     "rope_problem",
     "swiglu_problem",
     "ce_problem",
+    "block_problem",
+    "BLOCK_SIZES",
     "WORKLOADS",
 ]
 
@@ -133,6 +135,53 @@ def ce_problem(M: int, K: int, V: int, seed: int = 0) -> dict:
     }
 
 
+def block_problem(M: int, d: int, F: int, seed: int = 0, with_bwd: bool = True) -> dict:
+    """One period of the block-level chain: two GEMM-residual-RMSNorm-GEMM
+    structures (RoPE path, then SwiGLU path).
+
+    Tensors, in spawn order:
+      P[M,F] ~ N(0,1)        activation entering the down projection
+      Wd[F,d] ~ N(0,1/F)     down projection
+      x[M,d] ~ N(0,1)        residual stream entering the block
+      gamma1[d] ~ 1 + 0.1 N(0,1)
+      Wqkv[d,3d] ~ N(0,1/d)  QKV projection
+      O[M,d] ~ N(0,1)        attention-core output (the attention core itself is not part of the chain)
+      Wo[d,d] ~ N(0,1/d)     attention output projection
+      gamma2[d] ~ 1 + 0.1 N(0,1)
+      Wgu[d,2F] ~ N(0,1/d)   gate/up projection, gate and up columns interleaved
+    and for the backward:
+      dQKV[M,3d] ~ N(0,1)    gradient of the rotated QKV (from the attention backward)
+      gh[M,d] ~ N(0,1)       gradient of the next period's residual output
+      Wdn[F,d] ~ N(0,1/F)    the next period's down projection
+    """
+    g = _children(seed, 12)
+    out = {
+        "P": normal_bf16(g[0], (M, F)),
+        "Wd": normal_bf16(g[1], (F, d), std=1.0 / np.sqrt(F)),
+        "x": normal_bf16(g[2], (M, d)),
+        "gamma1": normal_bf16(g[3], (d,), std=0.1, mean=1.0),
+        "Wqkv": normal_bf16(g[4], (d, 3 * d), std=1.0 / np.sqrt(d)),
+        "O": normal_bf16(g[5], (M, d)),
+        "Wo": normal_bf16(g[6], (d, d), std=1.0 / np.sqrt(d)),
+        "gamma2": normal_bf16(g[7], (d,), std=0.1, mean=1.0),
+        "Wgu": normal_bf16(g[8], (d, 2 * F), std=1.0 / np.sqrt(d)),
+    }
+    if with_bwd:
+        out["dQKV"] = normal_bf16(g[9], (M, 3 * d))
+        out["gh"] = normal_bf16(g[10], (M, d))
+        out["Wdn"] = normal_bf16(g[11], (F, d), std=1.0 / np.sqrt(F))
+    return out
+
+
+# Block-level chain sizes: 16K tokens at the hidden widths of the 1B, 7B and
+# 70B model scales; F and head_dim as in Llama-3-family models of those widths;
+# positions = row mod 4096 (four 4096-token sequences).
+BLOCK_SIZES = {
+    2048: dict(M=16384, d=2048, F=8192, head_dim=64),
+    4096: dict(M=16384, d=4096, F=14336, head_dim=128),
+    8192: dict(M=16384, d=8192, F=28672, head_dim=128),
+}
+
 # The five workloads, by name, with their full sizes.
 WORKLOADS = {
     "rmsnorm_chain_tiny": dict(kind="rms_chain", M=256, K=512, d=512, N2=512, eps=1e-6),
@@ -143,3 +192,5 @@ WORKLOADS = {
                                bwd_K=8192),
     "lm_head_ce_8192": dict(kind="ce", M=8192, K=4096, V=32768),
 }
+for _d, _b in BLOCK_SIZES.items():
+    WORKLOADS[f"block_d{_d}"] = dict(kind="block", S=4096, theta=10000.0, eps=1e-6, rope_cols=2 * _d, **_b)

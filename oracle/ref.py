@@ -44,6 +44,17 @@ __all__ = [
     "ce_bwd",
     "gemm_ce_fwd",
     "gemm_ce_bwd",
+    # Block-level chain
+    "rmsnorm_bwd_textbook",
+    "gemm_rowscale_rope",
+    "gemm_rowscale_swiglu",
+    "gemm_swiglu_bwd_rowdot",
+    "gemm_rmsnorm_bwd_res",
+    "rope_bwd_rowdot",
+    "block_fwd",
+    "block_bwd",
+    "block_fwd_fused",
+    "block_bwd_fused",
 ]
 
 
@@ -367,3 +378,163 @@ def gemm_ce_bwd(H, W, labels, lse, grad_scale: float) -> dict:
     L = matmul(H, W)
     dl = ce_bwd(L, labels, lse, grad_scale)
     return dict(dl=dl, dH=matmul(dl, np.asarray(W, np.float64).T), dW=matmul(np.asarray(H, np.float64).T, dl))
+
+
+# ----------------------------------------------------------------------------
+# Block-level chain (CODA note, ablation on full Transformer blocks: two
+# consecutive GEMM-Residual-RMSNorm-GEMM structures, one covering the RoPE
+# path and one the SwiGLU path, with the light auxiliary reductions and glue).
+#
+# One period of a pre-norm layer stack, with the attention core left out (its
+# output O is an input, and the gradient of the rotated QKV arrives as dQKV):
+#   RoPE path:   h1 = P Wd + x;   n1 = RMSNorm(h1, gamma1);  QKV = RoPE(n1 Wqkv)
+#   SwiGLU path: h2 = O Wo + h1;  n2 = RMSNorm(h2, gamma2);  GU = n2 Wgu;
+#                A = SwiGLU(GU)
+# The backward takes the gradient of the rotated QKV (dQKV) and of the next
+# period's residual output h1' = A Wdn + h2 (gh), i.e. it differentiates
+#   L = <dQKV, QKV> + <gh, A Wdn + h2>.
+# ----------------------------------------------------------------------------
+
+def rmsnorm_bwd_textbook(dn, u, gamma, r) -> dict:
+    """Textbook RMSNorm backward through n = r u (.) gamma, r = (mean(u^2)+eps)^(-1/2):
+    ``du = r gamma (.) dn - r^3 u (1/d) rowsum(dn (.) gamma (.) u)`` and
+    ``dgamma_j = sum_i dn[i,j] r_i u[i,j]``."""
+    dn = np.asarray(dn, np.float64)
+    u = np.asarray(u, np.float64)
+    gamma = np.asarray(gamma, np.float64)
+    r = np.asarray(r, np.float64)
+    d = u.shape[1]
+    c = np.sum(dn * gamma[None, :] * u, axis=1) / d
+    du = r[:, None] * gamma[None, :] * dn - (r ** 3 * c)[:, None] * u
+    return dict(du=du, dgamma=np.sum(dn * r[:, None] * u, axis=0))
+
+
+def gemm_rowscale_rope(X, W, r, positions, head_dim: int, theta: float, rope_cols: int) -> np.ndarray:
+    """Second GEMM of the RoPE-path structure: the delayed row scale and the
+    rotation in one epilogue, ``QKV = RoPE(r (.)row (X W))`` (CODA note, Key
+    designs 1 and 2; r commutes with the right multiply and with the
+    rotation, which is linear per row)."""
+    return rope(rowscale(X, W, r), positions, head_dim, theta, rope_cols)
+
+
+def gemm_rowscale_swiglu(X, Wgu, r) -> dict:
+    """Second GEMM of the SwiGLU-path structure: ``GU = r (.)row (X Wgu)``,
+    ``A = SwiGLU(GU)`` (the scale precedes the nonlinearity)."""
+    GU = rowscale(X, Wgu, r)
+    return dict(GU=GU, A=swiglu(GU))
+
+
+def gemm_swiglu_bwd_rowdot(dY, Wd, GU, r, d: int) -> dict:
+    """SwiGLU-backward GEMM of the chain, with the RMSNorm-backward row
+    statistic in the same epilogue (CODA note, Key design 3: s is formed in
+    the GEMM that produces the gradient of the rowscale GEMM's output GU):
+    dA = dY Wd^T; dGU = swiglu_bwd(dA, GU); s = (1/d) rowsum(dGU (.) GU);
+    dGUr = r (.)row dGU."""
+    dA = matmul(dY, np.asarray(Wd, np.float64).T)
+    dGU = swiglu_bwd(dA, GU)
+    return dict(dA=dA, dGU=dGU, dGUr=np.asarray(r, np.float64)[:, None] * dGU, s=rowdot_stat(dGU, GU, d))
+
+
+def gemm_rmsnorm_bwd_res(dYr, W1, h, gamma, r, s, dres) -> dict:
+    """RMSNorm backward in the data-gradient GEMM, fed with the row-scaled
+    gradient: ``Gr = dYr W1^T = r (.)row G``, so ``dh = gamma (.) Gr -
+    r^2 s h + dres`` (the r^2 form of ``rmsnorm_bwd`` with G = Gr / r) where
+    dres is the gradient reaching h through the residual connection, and
+    ``dgamma_j = sum_i Gr[i,j] h[i,j]``."""
+    Gr = matmul(dYr, np.asarray(W1, np.float64).T)
+    r = np.asarray(r, np.float64)
+    b = rmsnorm_bwd(Gr / r[:, None], h, gamma, r, s)
+    return dict(Gr=Gr, dh=b["dh1"] + np.asarray(dres, np.float64), dgamma=b["dgamma"])
+
+
+def rope_bwd_rowdot(dQKV, QKV, r, positions, head_dim: int, theta: float, rope_cols: int, d: int) -> dict:
+    """Glue of the RoPE-path backward, on the gradient the attention backward
+    delivers: dYq = RoPE^T(dQKV) (the gradient of the unrotated QKV
+    projection Yq), the row statistic ``s = (1/d) rowsum(dYq (.) Yq)`` with
+    Yq = RoPE^T(QKV) recovered from the stored rotated output, and
+    ``dYqr = r (.)row dYq``."""
+    dYq = rope_bwd(dQKV, positions, head_dim, theta, rope_cols)
+    Yq = rope_bwd(QKV, positions, head_dim, theta, rope_cols)
+    return dict(dYq=dYq, dYqr=np.asarray(r, np.float64)[:, None] * dYq, s=rowdot_stat(dYq, Yq, d))
+
+
+def block_fwd(P, Wd, x, gamma1, Wqkv, O, Wo, gamma2, Wgu, positions, head_dim: int, theta: float,
+              rope_cols: int, eps: float) -> dict:
+    """Unfused definition of one period of the chain (see the section header).
+    Also reports the reparameterised intermediates h1g = h1 (.) gamma1 and
+    h2g = h2 (.) gamma2."""
+    g1 = np.asarray(gamma1, np.float64)
+    g2 = np.asarray(gamma2, np.float64)
+    h1 = matmul(P, Wd) + np.asarray(x, np.float64)
+    n1, r1 = rmsnorm(h1, g1, eps)
+    Yq = matmul(n1, Wqkv)
+    QKV = rope(Yq, positions, head_dim, theta, rope_cols)
+    h2 = matmul(O, Wo) + h1
+    n2, r2 = rmsnorm(h2, g2, eps)
+    GU = matmul(n2, Wgu)
+    return dict(h1=h1, n1=n1, r1=r1, Yq=Yq, QKV=QKV, h2=h2, n2=n2, r2=r2, GU=GU, A=swiglu(GU),
+                h1g=h1 * g1[None, :], h2g=h2 * g2[None, :])
+
+
+def block_bwd(P, Wd, x, gamma1, Wqkv, O, Wo, gamma2, Wgu, positions, head_dim: int, theta: float,
+              rope_cols: int, eps: float, dQKV, gh, Wdn) -> dict:
+    """Backward of one period by the plain chain rule (textbook RMSNorm
+    backward, no row statistic). dP = dh1 Wd^T is the gradient sent to the
+    previous period; in a chain its GEMM is the previous period's
+    SwiGLU-backward GEMM."""
+    f = block_fwd(P, Wd, x, gamma1, Wqkv, O, Wo, gamma2, Wgu, positions, head_dim, theta, rope_cols, eps)
+    gh = np.asarray(gh, np.float64)
+    dA = matmul(gh, np.asarray(Wdn, np.float64).T)
+    dGU = swiglu_bwd(dA, f["GU"])
+    dn2 = matmul(dGU, np.asarray(Wgu, np.float64).T)
+    b2 = rmsnorm_bwd_textbook(dn2, f["h2"], gamma2, f["r2"])
+    dh2 = b2["du"] + gh
+    dYq = rope_bwd(dQKV, positions, head_dim, theta, rope_cols)
+    dn1 = matmul(dYq, np.asarray(Wqkv, np.float64).T)
+    b1 = rmsnorm_bwd_textbook(dn1, f["h1"], gamma1, f["r1"])
+    dh1 = b1["du"] + dh2
+    return dict(
+        fwd=f, dA=dA, dGU=dGU, dn2=dn2, dh2=dh2, dgamma2=b2["dgamma"], dWgu=matmul(f["n2"].T, dGU),
+        dO=matmul(dh2, np.asarray(Wo, np.float64).T), dWo=matmul(np.asarray(O, np.float64).T, dh2),
+        dYq=dYq, dn1=dn1, dh1=dh1, dx=dh1, dgamma1=b1["dgamma"], dWqkv=matmul(f["n1"].T, dYq),
+        dWd=matmul(np.asarray(P, np.float64).T, dh1), dP=matmul(dh1, np.asarray(Wd, np.float64).T),
+    )
+
+
+def block_fwd_fused(P, Wd, x, gamma1, Wqkv, O, Wo, gamma2, Wgu, positions, head_dim: int, theta: float,
+                    rope_cols: int, eps: float) -> dict:
+    """The reparameterised forward, step by step as the fused kernels run it:
+    residual + RMS-prep GEMM, aux reduction of the sums of squares, rowscale
+    GEMM with the pair map, for each of the two structures."""
+    d = np.asarray(x).shape[1]
+    a = res_rmsprep(P, Wd, x, gamma1)
+    r1 = rms_reduce(a["sumsq"][:, None], d, eps)
+    QKV = gemm_rowscale_rope(a["h2"], Wqkv, r1, positions, head_dim, theta, rope_cols)
+    b = res_rmsprep(O, Wo, a["h1"], gamma2)
+    r2 = rms_reduce(b["sumsq"][:, None], d, eps)
+    s = gemm_rowscale_swiglu(b["h2"], Wgu, r2)
+    return dict(h1=a["h1"], h1g=a["h2"], r1=r1, QKV=QKV, h2=b["h1"], h2g=b["h2"], r2=r2, GU=s["GU"], A=s["A"])
+
+
+def block_bwd_fused(fused_fwd: dict, P, Wqkv, O, Wo, gamma1, gamma2, Wgu, positions, head_dim: int,
+                    theta: float, rope_cols: int, dQKV, gh, Wdn) -> dict:
+    """The reparameterised backward, step by step as the fused kernels run
+    it, from the fused forward's saved tensors: SwiGLU-backward GEMM with the
+    row statistic; RMSNorm-backward GEMM with the residual gradient; the
+    RoPE-path glue (transposed rotation, row statistic, row scale); the
+    second RMSNorm-backward GEMM; the weight-gradient GEMMs on the row-scaled
+    gradients."""
+    f = fused_fwd
+    d = f["h1"].shape[1]
+    b1 = gemm_swiglu_bwd_rowdot(gh, Wdn, f["GU"], f["r2"], d)
+    b3 = gemm_rmsnorm_bwd_res(b1["dGUr"], Wgu, f["h2"], gamma2, f["r2"], b1["s"], gh)
+    dh2 = b3["dh"]
+    g = rope_bwd_rowdot(dQKV, f["QKV"], f["r1"], positions, head_dim, theta, rope_cols, d)
+    b10 = gemm_rmsnorm_bwd_res(g["dYqr"], Wqkv, f["h1"], gamma1, f["r1"], g["s"], dh2)
+    dh1 = b10["dh"]
+    return dict(
+        dGUr=b1["dGUr"], s2=b1["s"], dh2=dh2, dgamma2=b3["dgamma"], dWgu=matmul(f["h2g"].T, b1["dGUr"]),
+        dO=matmul(dh2, np.asarray(Wo, np.float64).T), dWo=matmul(np.asarray(O, np.float64).T, dh2),
+        dYqr=g["dYqr"], s1=g["s"], dh1=dh1, dgamma1=b10["dgamma"], dWqkv=matmul(f["h1g"].T, g["dYqr"]),
+        dWd=matmul(np.asarray(P, np.float64).T, dh1),
+    )

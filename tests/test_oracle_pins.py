@@ -487,3 +487,166 @@ def test_inputs_bf16_rounding_and_determinism():
         assert np.array_equal(a[k], b[k])
     x = O.bf16(gen.rms_chain(512, 64, 64, 8)["x"])
     assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
+
+
+# ---------------------------------------------------------------------------
+# Block-level chain: one period of two GEMM-residual-RMSNorm-GEMM structures
+# (RoPE path, then SwiGLU path). The plain definition is pinned to a torch
+# float64 restatement (library rms_norm and silu, RoPE as a complex product)
+# and to autograd and finite differences of the scalar
+#   L = <dQKV, QKV> + <gh, A Wdn + h2>;
+# the reparameterised, kernel-by-kernel composition is then pinned to it.
+# ---------------------------------------------------------------------------
+
+BLK = dict(M=6, d=16, F=12, hd=8, rope_cols=32, theta=10000.0, eps=1e-6)
+
+
+def _block(seed=81, **kw):
+    c = dict(BLK, **kw)
+    R = rng(seed)
+    M, d, F = c["M"], c["d"], c["F"]
+    t = dict(
+        P=R.standard_normal((M, F)), Wd=R.standard_normal((F, d)) / np.sqrt(F), x=R.standard_normal((M, d)),
+        gamma1=1 + 0.1 * R.standard_normal(d), Wqkv=R.standard_normal((d, 3 * d)) / np.sqrt(d),
+        O=R.standard_normal((M, d)), Wo=R.standard_normal((d, d)) / np.sqrt(d),
+        gamma2=1 + 0.1 * R.standard_normal(d), Wgu=R.standard_normal((d, 2 * F)) / np.sqrt(d),
+    )
+    g = dict(dQKV=R.standard_normal((M, 3 * d)), gh=R.standard_normal((M, d)),
+             Wdn=R.standard_normal((F, d)) / np.sqrt(F))
+    pos = np.array([0, 1, 5, 17, 4095, 300])[:M]
+    return c, t, g, pos
+
+
+def _fwd_args(c, t, pos):
+    return (t["P"], t["Wd"], t["x"], t["gamma1"], t["Wqkv"], t["O"], t["Wo"], t["gamma2"], t["Wgu"], pos,
+            c["hd"], c["theta"], c["rope_cols"], c["eps"])
+
+
+def _torch_block(c, T, pos):
+    """Torch float64 restatement: rms_norm and silu from the library, the
+    rotation as multiplication by exp(i angle) on complex pairs."""
+    d = T["x"].shape[1]
+
+    def rope_t(Y):
+        hd, rc = c["hd"], c["rope_cols"]
+        i = torch.arange(hd // 2, dtype=torch.float64)
+        ang = torch.tensor(pos, dtype=torch.float64)[:, None] * c["theta"] ** (-2.0 * i / hd)[None, :]
+        rot = torch.polar(torch.ones_like(ang), ang)                      # [M, hd/2]
+        q = Y[:, :rc].reshape(Y.shape[0], rc // hd, hd // 2, 2)
+        z = torch.view_as_complex(q.contiguous()) * rot[:, None, :]
+        return torch.cat([torch.view_as_real(z).reshape(Y.shape[0], rc), Y[:, rc:]], dim=1)
+
+    h1 = T["P"] @ T["Wd"] + T["x"]
+    n1 = F.rms_norm(h1, (d,), T["gamma1"], c["eps"])
+    QKV = rope_t(n1 @ T["Wqkv"])
+    h2 = T["O"] @ T["Wo"] + h1
+    n2 = F.rms_norm(h2, (d,), T["gamma2"], c["eps"])
+    GU = n2 @ T["Wgu"]
+    A = F.silu(GU[:, 0::2]) * GU[:, 1::2]
+    return QKV, h2, A
+
+
+def test_block_fwd_matches_torch():
+    c, t, _, pos = _block()
+    f = O.block_fwd(*_fwd_args(c, t, pos))
+    QKV, h2, A = _torch_block(c, {k: t64(v) for k, v in t.items()}, pos)
+    assert rel(f["QKV"], QKV.numpy()) < 1e-13
+    assert rel(f["h2"], h2.numpy()) < 1e-13
+    assert rel(f["A"], A.numpy()) < 1e-13
+    assert np.array_equal(f["QKV"][:, c["rope_cols"]:], f["Yq"][:, c["rope_cols"]:])  # V passes through
+
+
+def test_block_bwd_matches_autograd():
+    c, t, g, pos = _block()
+    b = O.block_bwd(*_fwd_args(c, t, pos), g["dQKV"], g["gh"], g["Wdn"])
+    T = {k: t64(v, grad=True) for k, v in t.items()}
+    QKV, h2, A = _torch_block(c, T, pos)
+    L = torch.sum(t64(g["dQKV"]) * QKV) + torch.sum(t64(g["gh"]) * (A @ t64(g["Wdn"]) + h2))
+    L.backward()
+    for ours, theirs in [("dP", "P"), ("dx", "x"), ("dO", "O"), ("dWd", "Wd"), ("dgamma1", "gamma1"),
+                         ("dWqkv", "Wqkv"), ("dWo", "Wo"), ("dgamma2", "gamma2"), ("dWgu", "Wgu")]:
+        assert rel(b[ours], T[theirs].grad.numpy()) < 1e-12, ours
+
+
+def test_block_bwd_finite_differences():
+    c, t, g, pos = _block(seed=82, M=3, d=8, F=6, hd=8, rope_cols=16)
+
+    def loss(tt):
+        f = O.block_fwd(*_fwd_args(c, tt, pos))
+        return np.sum(g["dQKV"] * f["QKV"]) + np.sum(g["gh"] * (O.matmul(f["A"], g["Wdn"]) + f["h2"]))
+
+    b = O.block_bwd(*_fwd_args(c, t, pos), g["dQKV"], g["gh"], g["Wdn"])
+    h = 1e-6
+    for name, grad in [("gamma1", "dgamma1"), ("gamma2", "dgamma2"), ("x", "dx"), ("Wd", "dWd"), ("O", "dO")]:
+        num = np.zeros_like(t[name])
+        for idx in np.ndindex(t[name].shape):
+            a = {k: v.copy() for k, v in t.items()}
+            m = {k: v.copy() for k, v in t.items()}
+            a[name][idx] += h
+            m[name][idx] -= h
+            num[idx] = (loss(a) - loss(m)) / (2 * h)
+        assert rel(b[grad], num) < 1e-7, name
+
+
+def test_block_fused_composition_equals_definition():
+    c, t, g, pos = _block(seed=83)
+    args = _fwd_args(c, t, pos)
+    f = O.block_fwd(*args)
+    ff = O.block_fwd_fused(*args)
+    for k in ("h1", "h1g", "r1", "QKV", "h2", "h2g", "r2", "GU", "A"):
+        assert rel(ff[k], f[k]) < 1e-13, k
+    b = O.block_bwd(*args, g["dQKV"], g["gh"], g["Wdn"])
+    bf = O.block_bwd_fused(ff, t["P"], t["Wqkv"], t["O"], t["Wo"], t["gamma1"], t["gamma2"], t["Wgu"], pos,
+                           c["hd"], c["theta"], c["rope_cols"], g["dQKV"], g["gh"], g["Wdn"])
+    for k in ("dh2", "dgamma2", "dWgu", "dO", "dWo", "dh1", "dgamma1", "dWqkv", "dWd"):
+        assert rel(bf[k], b[k]) < 1e-12, k
+    # the row statistics are the textbook (1/d) rowsum(dn (.) gamma (.) h) scaled by r
+    d = c["d"]
+    assert rel(bf["s2"], f["r2"] * np.sum(b["dn2"] * t["gamma2"] * f["h2"], axis=1) / d) < 1e-12
+    assert rel(bf["s1"], f["r1"] * np.sum(b["dn1"] * t["gamma1"] * f["h1"], axis=1) / d) < 1e-12
+
+
+def test_block_kernel_pieces():
+    c, t, g, pos = _block(seed=84)
+    R = rng(85)
+    M, d = c["M"], c["d"]
+    X = R.standard_normal((M, d))
+    r = 0.5 + R.random(M)
+    # rowscale commutes with the rotation and feeds the SwiGLU pair map unchanged
+    q = O.gemm_rowscale_rope(X, t["Wqkv"], r, pos, c["hd"], c["theta"], c["rope_cols"])
+    assert rel(q, r[:, None] * O.gemm_rope(X, t["Wqkv"], pos, c["hd"], c["theta"], c["rope_cols"])) < 1e-13
+    s = O.gemm_rowscale_swiglu(X, t["Wgu"], r)
+    assert rel(s["GU"], r[:, None] * (X @ t["Wgu"])) < 1e-13
+    assert rel(s["A"], O.swiglu(s["GU"])) == 0.0
+    # the RoPE glue's statistic is rotation invariant: it equals (1/d) rowsum(dQKV (.) QKV)
+    QKV = R.standard_normal((M, 3 * d))
+    gl = O.rope_bwd_rowdot(g["dQKV"], QKV, r, pos, c["hd"], c["theta"], c["rope_cols"], d)
+    assert rel(gl["s"], np.sum(g["dQKV"] * QKV, axis=1) / d) < 1e-13
+    assert rel(gl["dYqr"], r[:, None] * O.rope_bwd(g["dQKV"], pos, c["hd"], c["theta"], c["rope_cols"])) < 1e-14
+    # the residual gradient is additive; with dres = 0 it is the plain RMSNorm-backward GEMM on dYr / r
+    dYr = R.standard_normal((M, 2 * c["F"]))
+    h = R.standard_normal((M, d))
+    sv = R.standard_normal(M)
+    dres = R.standard_normal((M, d))
+    a = O.gemm_rmsnorm_bwd_res(dYr, t["Wgu"], h, t["gamma2"], r, sv, dres)
+    z = O.gemm_rmsnorm_bwd_res(dYr, t["Wgu"], h, t["gamma2"], r, sv, np.zeros_like(dres))
+    p = O.gemm_rmsnorm_bwd(dYr / r[:, None], t["Wgu"], h, t["gamma2"], r, sv)
+    assert rel(a["dh"] - dres, z["dh"]) < 1e-13
+    assert rel(z["dh"], p["dh1"]) < 1e-13 and rel(z["dgamma"], p["dgamma"]) < 1e-13
+    # SwiGLU-backward GEMM with the row statistic: s over the 2F pre-activation columns, over d
+    sb = O.gemm_swiglu_bwd_rowdot(g["gh"], g["Wdn"], s["GU"], r, d)
+    assert rel(sb["dGU"], O.gemm_swiglu_bwd(g["gh"], g["Wdn"], s["GU"])["dGU"]) < 1e-14
+    assert rel(sb["s"], np.sum(sb["dGU"] * s["GU"], axis=1) / d) < 1e-14
+
+
+def test_block_inputs_generator():
+    a = gen.block_problem(8, 16, 24, seed=3)
+    b = gen.block_problem(8, 16, 24, seed=3, with_bwd=False)
+    assert set(a) - set(b) == {"dQKV", "gh", "Wdn"}
+    for k in b:
+        assert np.array_equal(a[k], b[k])
+    shapes = dict(P=(8, 24), Wd=(24, 16), x=(8, 16), gamma1=(16,), Wqkv=(16, 48), O=(8, 16), Wo=(16, 16),
+                  gamma2=(16,), Wgu=(16, 48), dQKV=(8, 48), gh=(8, 16), Wdn=(24, 16))
+    assert {k: v.shape for k, v in a.items()} == shapes
+    w = O.bf16(gen.block_problem(64, 256, 512, with_bwd=False)["Wgu"])
+    assert abs(w.std() * 16 - 1) < 0.02
