@@ -23,7 +23,9 @@ __all__ = [
     "coda_rowdot_reduce", "coda_gemm_rmsnorm_bwd", "coda_colsum_reduce", "coda_unfused_add",
     "coda_unfused_rmsnorm", "coda_unfused_rowscale", "coda_unfused_swiglu", "coda_unfused_swiglu_bwd",
     "coda_unfused_rope", "coda_unfused_rope_bwd", "coda_unfused_ce_fwd", "coda_unfused_ce_bwd",
-    "coda_unfused_rowdot", "coda_unfused_rmsnorm_bwd",
+    "coda_unfused_rowdot", "coda_unfused_rmsnorm_bwd", "coda_gemm_rowscale_rope", "coda_gemm_rowscale_swiglu",
+    "coda_gemm_swiglu_bwd_rowdot", "coda_gemm_rmsnorm_bwd_res", "coda_rope_bwd_rowdot",
+    "coda_block_workspace_bytes", "CodaBlock",
 ]
 
 
@@ -388,3 +390,149 @@ def coda_unfused_rmsnorm_bwd(G, h, gamma, r, stream=None):
     _check(lib().coda_unfused_rmsnorm_bwd(M, d, _ptr(G), _ptr(h), _ptr(gamma), _ptr(r), _ptr(dh), _ptr(pdg),
                                           _stream(stream)))
     return dh, pdg
+
+
+# ----------------------------------------------------------------- block-level chain
+
+def coda_gemm_rowscale_rope(X, W, r, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
+    """out = RoPE(r * (X W)) (row scale and rotation in one epilogue)."""
+    _bf16(X, "X", 2), _bf16(W, "W", 2), _f32(r, "r"), _f32(cos, "cos"), _f32(sin, "sin")
+    M, K = X.shape
+    N = W.shape[1]
+    if W.shape[0] != K or r.shape[0] != M or cos.shape != sin.shape or cos.shape[1] != head_dim // 2:
+        raise ValueError("shape mismatch")
+    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    _check(lib().coda_gemm_rowscale_rope(M, N, K, _ptr(X), _ptr(W), _ptr(r), _ptr(cos), _ptr(sin), cos.shape[0],
+                                         head_dim, rope_cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_rowscale_swiglu(X, Wgu, r, want_gu: bool = False, out=None, gu=None, stream=None):
+    """GU = r * (X Wgu), A = silu(G) * U; returns (A, GU or None)."""
+    _bf16(X, "X", 2), _bf16(Wgu, "Wgu", 2), _f32(r, "r")
+    M, K = X.shape
+    F2 = Wgu.shape[1]
+    if Wgu.shape[0] != K or F2 % 2 or r.shape[0] != M:
+        raise ValueError("shape mismatch")
+    F = F2 // 2
+    out = _empty((M, F), torch.bfloat16, X) if out is None else out
+    if want_gu and gu is None:
+        gu = _empty((M, F2), torch.bfloat16, X)
+    _check(lib().coda_gemm_rowscale_swiglu(M, F, K, _ptr(X), _ptr(Wgu), _ptr(r), _ptr(out), _ptr(gu),
+                                           _stream(stream)))
+    return out, gu
+
+
+def coda_gemm_swiglu_bwd_rowdot(dY, Wd, gu, r, stream=None):
+    """dGUr = r * SwiGLU'(dY Wd^T; gu) and the row-statistic partials of dGU * gu.
+    Returns (dgur [M,2F], pdot [M, ceil(F/128)])."""
+    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2), _bf16(gu, "gu", 2), _f32(r, "r")
+    M, K = dY.shape
+    F = Wd.shape[0]
+    if Wd.shape[1] != K or gu.shape != (M, 2 * F) or r.shape[0] != M:
+        raise ValueError("shape mismatch")
+    dgur = _empty((M, 2 * F), torch.bfloat16, dY)
+    pdot = _empty((M, coda_num_col_tiles(F)), torch.float32, dY)
+    _check(lib().coda_gemm_swiglu_bwd_rowdot(M, F, K, _ptr(dY), _ptr(Wd), _ptr(gu), _ptr(r), _ptr(dgur), _ptr(pdot),
+                                             _stream(stream)))
+    return dgur, pdot
+
+
+def coda_gemm_rmsnorm_bwd_res(dYr, W1, h, gamma, r, s, dres, stream=None):
+    """dh = gamma * (dYr W1^T) - r^2 s h + dres (W1 stored [d, K]); returns (dh, pdg)."""
+    _bf16(dYr, "dYr", 2), _bf16(W1, "W1", 2), _bf16(h, "h", 2), _bf16(gamma, "gamma", 1), _bf16(dres, "dres", 2)
+    _f32(r, "r"), _f32(s, "s")
+    M, K = dYr.shape
+    d = W1.shape[0]
+    if W1.shape[1] != K or h.shape != (M, d) or dres.shape != (M, d):
+        raise ValueError("shape mismatch")
+    dh = _empty((M, d), torch.bfloat16, dYr)
+    pdg = _empty((coda_num_row_tiles(M), d), torch.float32, dYr)
+    _check(lib().coda_gemm_rmsnorm_bwd_res(M, d, K, _ptr(dYr), _ptr(W1), _ptr(h), _ptr(gamma), _ptr(r), _ptr(s),
+                                           _ptr(dres), _ptr(dh), _ptr(pdg), _stream(stream)))
+    return dh, pdg
+
+
+def coda_rope_bwd_rowdot(dqkv, qkv, r, cos, sin, head_dim: int, rope_cols: int, d: int, stream=None):
+    """dqr = r * RoPE^T(dqkv), s = (1/d) rowsum(dqkv * qkv); returns (dqr, s)."""
+    _bf16(dqkv, "dqkv", 2), _bf16(qkv, "qkv", 2), _f32(r, "r"), _f32(cos, "cos"), _f32(sin, "sin")
+    M, N = dqkv.shape
+    if qkv.shape != (M, N) or r.shape[0] != M:
+        raise ValueError("shape mismatch")
+    dqr = torch.empty_like(dqkv)
+    s = _empty((M,), torch.float32, dqkv)
+    _check(lib().coda_rope_bwd_rowdot(M, N, _ptr(dqkv), _ptr(qkv), _ptr(r), _ptr(cos), _ptr(sin), cos.shape[0],
+                                      head_dim, rope_cols, d, _ptr(dqr), _ptr(s), _stream(stream)))
+    return dqr, s
+
+
+def coda_block_workspace_bytes(M: int, d: int, F: int, unfused: bool = False) -> int:
+    return int(lib().coda_block_workspace_bytes(M, d, F, int(unfused)))
+
+
+class CodaBlock:
+    """One period of the block-level chain (coda_block_t): the caller's inputs
+    and weights, and every saved tensor, output and scratch buffer, allocated
+    here with torch. ``fwd()``/``bwd()`` run the fused sequence,
+    ``fwd_unfused()``/``bwd_unfused()`` the unfused one (which rotates
+    ``dqkv`` in place). Field meanings are those of include/coda.h.
+
+    ``t``: dict of CUDA bf16 tensors P, x, O, Wd, gamma1, Wqkv, Wo, gamma2, Wgu
+    and, for the backward, dQKV, gh, Wdn.
+    """
+
+    _IN = ("P", "x", "O", "Wd", "gamma1", "Wqkv", "Wo", "gamma2", "Wgu")
+
+    def __init__(self, t: dict, head_dim: int, rope_cols: int, cos, sin, eps: float = 1e-6, unfused: bool = False):
+        for k in self._IN:
+            _bf16(t[k], k)
+        _f32(cos, "cos"), _f32(sin, "sin")
+        M, F = t["P"].shape
+        d = t["x"].shape[1]
+        dev = t["x"]
+        bf, f32 = torch.bfloat16, torch.float32
+        self.M, self.d, self.F = M, d, F
+        self.t = t
+        self.cos, self.sin = cos, sin
+        e = lambda *shape, dt=bf: _empty(shape, dt, dev)  # noqa: E731
+        self.h1, self.h1g, self.h2, self.h2g = e(M, d), e(M, d), e(M, d), e(M, d)
+        self.gu, self.r1, self.r2 = e(M, 2 * F), e(M, dt=f32), e(M, dt=f32)
+        self.qkv, self.a = e(M, 3 * d), e(M, F)
+        self.dh1, self.dh2, self.dO = e(M, d), e(M, d), e(M, d)
+        self.dWd, self.dWqkv, self.dWo, self.dWgu = e(F, d), e(d, 3 * d), e(d, d), e(d, 2 * F)
+        self.dgamma1, self.dgamma2 = e(d, dt=f32), e(d, dt=f32)
+        self.dgur, self.dqr = e(M, 2 * F), e(M, 3 * d)
+        self.s1, self.s2 = e(M, dt=f32), e(M, dt=f32)
+        nbytes = max(coda_block_workspace_bytes(M, d, F, unfused), coda_block_workspace_bytes(M, d, F, False))
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev.device)
+        ws = (self.workspace.data_ptr() + 255) & ~255
+        b = _lib.CodaBlock()
+        b.M, b.d, b.F, b.head_dim, b.rope_cols, b.S, b.eps = M, d, F, head_dim, rope_cols, cos.shape[0], float(eps)
+        b.cos_tab, b.sin_tab = _ptr(cos), _ptr(sin)
+        for k in self._IN:
+            setattr(b, k, _ptr(t[k]))
+        for k in ("h1", "h1g", "h2", "h2g", "gu", "r1", "r2", "qkv", "a", "dh1", "dh2", "dO", "dWd", "dWqkv", "dWo",
+                  "dWgu", "dgamma1", "dgamma2", "dgur", "dqr", "s1", "s2"):
+            setattr(b, k, _ptr(getattr(self, k)))
+        for k, f in (("dQKV", "dqkv"), ("gh", "gh"), ("Wdn", "Wdn")):
+            if k in t:
+                _bf16(t[k], k)
+                setattr(b, f, _ptr(t[k]))
+        b.workspace = ws
+        self._b = b
+
+    def _run(self, fname, stream):
+        _check(getattr(lib(), fname)(self._b, _stream(stream)))
+        return self
+
+    def fwd(self, stream=None):
+        return self._run("coda_block_fwd", stream)
+
+    def bwd(self, stream=None):
+        return self._run("coda_block_bwd", stream)
+
+    def fwd_unfused(self, stream=None):
+        return self._run("coda_block_fwd_unfused", stream)
+
+    def bwd_unfused(self, stream=None):
+        return self._run("coda_block_bwd_unfused", stream)

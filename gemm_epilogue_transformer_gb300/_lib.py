@@ -5,12 +5,33 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import c_double, c_float, c_int, c_uint64, c_void_p, c_char_p
+from ctypes import POINTER, Structure, c_char_p, c_double, c_float, c_int, c_size_t, c_uint64, c_void_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
 
 P = c_void_p  # any device pointer (bf16 / fp32 / int32) or stream handle
 I = c_int
+
+
+
+class CodaBlock(Structure):
+    """coda_block_t: descriptor of one period of the block-level chain (field
+    order and types as in include/coda.h)."""
+    _fields_ = [
+        ("M", c_int), ("d", c_int), ("F", c_int), ("head_dim", c_int), ("rope_cols", c_int), ("S", c_int),
+        ("eps", c_float), ("cos_tab", P), ("sin_tab", P),
+        ("P", P), ("x", P), ("O", P), ("Wd", P), ("gamma1", P), ("Wqkv", P), ("Wo", P), ("gamma2", P), ("Wgu", P),
+        ("h1", P), ("h1g", P), ("h2", P), ("h2g", P), ("gu", P), ("r1", P), ("r2", P),
+        ("qkv", P), ("a", P),
+        ("dqkv", P), ("gh", P), ("Wdn", P),
+        ("dh1", P), ("dh2", P), ("dO", P), ("dWd", P), ("dWqkv", P), ("dWo", P), ("dWgu", P),
+        ("dgamma1", P), ("dgamma2", P),
+        ("dgur", P), ("dqr", P), ("s1", P), ("s2", P),
+        ("workspace", P),
+    ]
+
+
+BLK = POINTER(CodaBlock)
 
 # name -> (restype, argtypes); mirrors include/coda.h
 SIGNATURES = {
@@ -49,6 +70,16 @@ SIGNATURES = {
     "coda_unfused_ce_bwd": (I, [I, I, P, P, P, c_float, P, P]),
     "coda_unfused_rowdot": (I, [I, I, I, P, P, P, P]),
     "coda_unfused_rmsnorm_bwd": (I, [I, I, P, P, P, P, P, P, P]),
+    "coda_gemm_rowscale_rope": (I, [I, I, I, P, P, P, P, P, I, I, I, P, P]),
+    "coda_gemm_rowscale_swiglu": (I, [I, I, I, P, P, P, P, P, P]),
+    "coda_gemm_swiglu_bwd_rowdot": (I, [I, I, I, P, P, P, P, P, P, P]),
+    "coda_gemm_rmsnorm_bwd_res": (I, [I, I, I, P, P, P, P, P, P, P, P, P, P]),
+    "coda_rope_bwd_rowdot": (I, [I, I, P, P, P, P, P, I, I, I, I, P, P, P]),
+    "coda_block_workspace_bytes": (c_size_t, [I, I, I, I]),
+    "coda_block_fwd": (I, [BLK, P]),
+    "coda_block_bwd": (I, [BLK, P]),
+    "coda_block_fwd_unfused": (I, [BLK, P]),
+    "coda_block_bwd_unfused": (I, [BLK, P]),
 }
 
 _lib = None

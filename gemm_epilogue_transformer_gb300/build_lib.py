@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcoda.so")
 
-SOURCES = ["runtime.cu", "aux.cu", "unfused.cu", "gemm_fwd.cu", "gemm_bwd.cu"]
+SOURCES = ["runtime.cu", "aux.cu", "unfused.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_chain.cu", "block.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

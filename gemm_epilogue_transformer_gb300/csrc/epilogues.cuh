@@ -171,21 +171,33 @@ struct EpiRowScale {
 // kSaveGU: also store the pre-activation GU (bf16) for the backward, one more
 // store box per chunk (a separate instantiation: the extra staging box costs
 // one mainloop stage, which the plain forward keeps).
-template <bool kSaveGU>
+// kScale: the delayed RMSNorm row scale of the block chain, GU = r[i] * acc,
+// applied before the pair map (CODA note, Key design 1 composed with Key
+// design 2); the saved GU is the scaled pre-activation.
+template <bool kSaveGU, bool kScale = false>
 struct EpiSwiGLU {
   struct Params {
     int unused;
+    const float* r;  // kScale only
   };
-  struct State {};
+  struct State {
+    float rv;
+  };
   CODA_NO_PREFETCH
   CODA_NO_INPUT
   static constexpr int kChunksPerStore = 2;
   static constexpr int kMaxSlots = kSaveGU ? 3 : 2;
   // slot 0: A (32 outputs from two chunks); slots 1, 2: GU of the two chunks
   __device__ static int slots(const Params&) { return kSaveGU ? 3 : 1; }
-  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
                                uint32_t, uint32_t box0, uint32_t) {
+    if constexpr (kScale) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] *= st.rv;
+    }
     if (kSaveGU) stage_row32(box0 + (1 + (c & 1)) * kStageBoxBytes, cx.lane, acc);
     float o[16];
 #pragma unroll
@@ -265,15 +277,21 @@ struct EpiSwiGLUBwd {
 // Adjacent pairs (2i, 2i+1) within each head of the first rope_cols columns,
 // position = row mod S, cos/sin from the caller's fp32 tables [S, head_dim/2].
 // kSign = +1: forward rotation; -1: transposed rotation (backward).
-template <int kSign>
+// kScale: the delayed RMSNorm row scale of the block chain, out = RoPE(r[i] *
+// acc) (CODA note, Key design 1 composed with Key design 2; the row scale
+// commutes with the per-row rotation).
+template <int kSign, bool kScale = false>
 struct EpiRope {
   struct Params {
     const float* cos_tab;
     const float* sin_tab;
     int S, head_dim, rope_cols;
     int tma_tables;  // 1: the cos/sin slices arrive by TMA (S % 32 == 0); 0: direct loads
+    const float* r;  // kScale only
   };
-  struct State {};
+  struct State {
+    float rv;
+  };
   struct Pre {
     uint4 c[4], s[4];
   };
@@ -306,10 +324,16 @@ struct EpiRope {
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
-  __device__ static void begin(State&, const Params&, const EpiCtx&) {}
-  __device__ static void chunk(State&, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
                                uint32_t in, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
+    if constexpr (kScale) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] *= st.rv;
+    }
     if (col0 < ep.rope_cols) {
       float cs[16], sn[16];
       uint4 tc[4], ts[4];
@@ -560,6 +584,138 @@ struct EpiRmsNormBwd {
     stage_row32(box0, cx.lane, acc);
     const float tot = warp_colsum32(part, cx.lane);
     // rows past M contribute zeros; a warp slice that starts past M has no partial row
+    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
+      ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
+  }
+  CODA_STORE_SAME_COLS(0)
+  __device__ static void end(State&, const Params&, const EpiCtx&) {}
+};
+
+// ------------------------------- SwiGLU backward with the row statistic
+// Block chain, SwiGLU path: acc = dA[:, f0..f0+31] from dA = gh Wdn^T. As
+// EpiSwiGLUBwd, plus the RMSNorm-backward row statistic of the rowscale GEMM
+// that produced GU (CODA note, Key design 3: s = (1/d) rowsum(dGU (.) GU)
+// formed in the GEMM that produces dGU; partial over the segment, fp32 dGU
+// times the loaded bf16 GU), and the output stored already row-scaled,
+// dGUr = r (.)row dGU, the form both consumers take (the weight gradient
+// h2g^T dGUr and the RMSNorm-backward GEMM on dGUr Wgu^T = r (.)row G).
+struct EpiSwiGLUBwdRowdot {
+  struct Params {
+    const __nv_bfloat16* gu;  // [M, 2F]
+    const float* r;           // [M]
+    float* pdot;              // [M, ceil(F/128)]
+  };
+  struct State {
+    float dot, rv;
+  };
+  CODA_NO_PREFETCH
+  static constexpr int kInBoxes = 2;
+  __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+    map = 0;
+    x = 2 * (cx.n0 + 32 * c) + 32 * b;
+    y = cx.wrow0;
+  }
+  static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
+  __device__ static int slots(const Params&) { return 2; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    st.dot = 0.f;
+    st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+  }
+  __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
+                               uint32_t in, uint32_t box0, uint32_t box1) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float g[32];
+      uint4 u[4];
+      box_row(in + half * kInBoxBytes, cx.lane, u);
+      unpack32(u, g);
+      float o[32];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float G = g[2 * k], U = g[2 * k + 1], dA = acc[16 * half + k];
+        const float sg = sigmoid_f(G);
+        const float dG = dA * U * sg * (1.0f + G * (1.0f - sg));
+        const float dU = dA * G * sg;
+        st.dot = fmaf(dG, G, st.dot);
+        st.dot = fmaf(dU, U, st.dot);
+        o[2 * k] = st.rv * dG;
+        o[2 * k + 1] = st.rv * dU;
+      }
+      stage_row32(half ? box1 : box0, cx.lane, o);
+    }
+  }
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
+    map = 0;
+    x = 2 * (cx.n0 + 32 * c) + 32 * s;
+    y = cx.wrow0;
+  }
+  __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot;
+  }
+};
+
+// -------------------- RMSNorm backward with the residual-stream gradient
+// Block chain: acc = Gr = dYr W^T = r (.)row G (the mainloop consumes the
+// row-scaled gradient). dh = gamma (.) Gr - r^2 s h + dres, where dres is the
+// gradient reaching h through the residual connection (a second input tile);
+// column partial of Gr h (= r G h) over the warp's 32 rows.
+struct EpiRmsNormBwdRes {
+  struct Params {
+    const __nv_bfloat16* h;
+    const __nv_bfloat16* gamma;
+    const float* r;
+    const float* s;
+    float* pdg;  // [ceil(M/32), d]
+  };
+  struct State {
+    float r2s;
+  };
+  struct Pre {
+    uint4 g[4];
+  };
+  __device__ static void prefetch(const Params& ep, const EpiCtx& cx, int c, Pre& pr) {
+    load_raw32(ep.gamma, 0, 1, cx.N, 0, cx.n0 + 32 * c, pr.g);
+  }
+  // box 0: h (map 0), box 1: dres (map 1), both the chunk's 32 x 32 tile
+  static constexpr int kInBoxes = 2;
+  __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+    map = b;
+    x = cx.n0 + 32 * c;
+    y = cx.wrow0;
+  }
+  static constexpr int kChunksPerStore = 1;
+  static constexpr int kMaxSlots = 2;
+  __device__ static int slots(const Params&) { return 1; }
+  __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
+    if (cx.row < cx.M) {
+      const float rv = ep.r[cx.row];
+      st.r2s = rv * rv * ep.s[cx.row];
+    } else {
+      st.r2s = 0.f;
+    }
+  }
+  __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
+                               uint32_t in, uint32_t box0, uint32_t) {
+    const int col0 = cx.n0 + 32 * c;
+    float h[32], g[32], part[32];
+    uint4 u[4];
+    box_row(in, cx.lane, u);
+    unpack32(u, h);
+    unpack32(pr.g, g);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      part[i] = acc[i] * h[i];
+      acc[i] = g[i] * acc[i] - st.r2s * h[i];
+    }
+    box_row(in + kInBoxBytes, cx.lane, u);
+    unpack32(u, h);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] += h[i];
+    stage_row32(box0, cx.lane, acc);
+    const float tot = warp_colsum32(part, cx.lane);
     if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
       ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
   }

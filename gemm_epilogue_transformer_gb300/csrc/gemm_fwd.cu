@@ -113,22 +113,6 @@ int coda_gemm_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* W
                                         as_stream(stream));
 }
 
-// TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16
-// frequencies (64 bytes) per box. Used when S % 32 == 0, so that a warp's 32
-// rows never wrap inside a box; otherwise the epilogue loads the tables directly.
-static int rope_table_maps(int tma, const float* c, const float* s, int S, int head_dim, const CUtensorMap& other,
-                           CUtensorMap* tc, CUtensorMap* ts) {
-  if (!tma) {
-    *tc = other;
-    *ts = other;
-    return CODA_OK;
-  }
-  const uint64_t half = static_cast<uint64_t>(head_dim / 2);
-  int rc = make_map_f32(tc, c, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (rc) return rc;
-  return make_map_f32(ts, s, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
 static int rope_common(const char* fn, int M, int N, int K, const coda_bf16* X, const coda_bf16* W,
                        const float* cos_tab, const float* sin_tab, int S, int head_dim, int rope_cols, coda_bf16* out) {
   int rc = check_fused(fn, M, N, K, X, W);

@@ -19,6 +19,22 @@ inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, in
                        static_cast<uint64_t>(ld) * 2u, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16
+// frequencies (64 bytes) per box. Used when S % 32 == 0, so that a warp's 32
+// rows never wrap inside a box; otherwise the epilogue loads the tables directly.
+inline int rope_table_maps(int tma, const float* c, const float* s, int S, int head_dim, const CUtensorMap& other,
+                           CUtensorMap* tc, CUtensorMap* ts) {
+  if (!tma) {
+    *tc = other;
+    *ts = other;
+    return CODA_OK;
+  }
+  const uint64_t half = static_cast<uint64_t>(head_dim / 2);
+  int rc = make_map_f32(tc, c, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc) return rc;
+  return make_map_f32(ts, s, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 template <class Epi, int kCG>
 int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, const void* A, int lda, int a_mn,
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,

@@ -273,6 +273,151 @@ int coda_unfused_rowdot(int M, int N, int d, const coda_bf16* dY, const coda_bf1
 int coda_unfused_rmsnorm_bwd(int M, int d, const coda_bf16* G, const coda_bf16* h, const coda_bf16* gamma,
                              const float* r, coda_bf16* dh_out, float* pdg_out, coda_stream_t stream);
 
+/* ------------------------------------------------------ block-level chain (f1)
+ * CODA note, block-level ablation: a Transformer block seen as two
+ * consecutive GEMM-Residual-RMSNorm-GEMM structures, one on the RoPE path and
+ * one on the SwiGLU path, with the light auxiliary reductions and glue. One
+ * period of a pre-norm layer stack, the attention core left out (its output O
+ * is an input; the attention backward's gradient of the rotated QKV, dQKV, is
+ * an input):
+ *   RoPE path:   h1 = P Wd + x;  n1 = RMSNorm(h1, gamma1);  QKV = RoPE(n1 Wqkv)
+ *   SwiGLU path: h2 = O Wo + h1; n2 = RMSNorm(h2, gamma2);  GU = n2 Wgu;
+ *                A = SwiGLU(GU)
+ * The backward differentiates L = <dQKV, QKV> + <gh, A Wdn + h2>, where gh is
+ * the gradient of the next period's residual output A Wdn + h2 and Wdn [F,d]
+ * the next period's down projection. The gradient of the block input P
+ * (dh1 Wd^T) is the next-earlier period's SwiGLU-backward GEMM and is not
+ * formed here.
+ *
+ * The four composed kernels below are used by the fused chain; each is also a
+ * stand-alone entry point. */
+
+/* coda_gemm_rowscale_rope: out = RoPE(r (.)row (X W)): the delayed row scale
+ *   (Key design 1) and the pair rotation (Key design 2) in one epilogue.
+ *   X [M,K], W [K,N], r [M] fp32, cos/sin [S, head_dim/2] -> out [M,N] bf16.
+ *   Rotation, positions and limits as coda_gemm_rope. */
+int coda_gemm_rowscale_rope(int M, int N, int K, const coda_bf16* X, const coda_bf16* W, const float* r,
+                            const float* cos_tab, const float* sin_tab, int S, int head_dim, int rope_cols,
+                            coda_bf16* out, coda_stream_t stream);
+
+/* coda_gemm_rowscale_swiglu: GU = r (.)row (X Wgu) (the scale precedes the
+ *   nonlinearity); A[:, f] = silu(GU[:, 2f]) GU[:, 2f+1]. gu_out (the scaled
+ *   pre-activation, [M,2F] bf16) may be NULL. Limits as coda_gemm_swiglu. */
+int coda_gemm_rowscale_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* Wgu, const float* r,
+                              coda_bf16* A_out, coda_bf16* gu_out, coda_stream_t stream);
+
+/* coda_gemm_swiglu_bwd_rowdot: dA = dY Wd^T (Wd stored [F,K]); the epilogue
+ *   forms dGU = SwiGLU'(dA; gu) as coda_gemm_swiglu_bwd, the RMSNorm-backward
+ *   row-statistic partials of the rowscale GEMM that produced gu (Key design 3),
+ *   pdot[i,t] = sum over the 256 gu columns of dA block t of dGU[i,j] gu[i,j]
+ *   (fp32 dGU times the stored bf16 gu), and stores dGUr = r (.)row dGU.
+ *   dY [M,K], Wd [F,K], gu [M,2F], r [M] -> dgur [M,2F] bf16,
+ *   pdot [M, coda_num_col_tiles(F)] fp32 (s = coda_rowdot_reduce(.., d, ..)). */
+int coda_gemm_swiglu_bwd_rowdot(int M, int F, int K, const coda_bf16* dY, const coda_bf16* Wd, const coda_bf16* gu,
+                                const float* r, coda_bf16* dgur_out, float* pdot_out, coda_stream_t stream);
+
+/* coda_gemm_rmsnorm_bwd_res: Gr = dYr W1^T (W1 stored [d,K]) on the row-scaled
+ *   gradient, so Gr = r (.)row G; epilogue dh = gamma (.) Gr - r^2 s h + dres
+ *   (dres: the gradient reaching h through the residual connection) and column
+ *   partials pdg[b,j] = sum over the rows of row tile b of Gr[i,j] h[i,j].
+ *   dYr [M,K], W1 [d,K], h, dres [M,d] bf16, gamma [d] bf16, r, s [M] ->
+ *   dh [M,d] bf16, pdg [coda_num_row_tiles(M), d] fp32. */
+int coda_gemm_rmsnorm_bwd_res(int M, int d, int K, const coda_bf16* dYr, const coda_bf16* W1, const coda_bf16* h,
+                              const coda_bf16* gamma, const float* r, const float* s, const coda_bf16* dres,
+                              coda_bf16* dh_out, float* pdg_out, coda_stream_t stream);
+
+/* coda_rope_bwd_rowdot: the RoPE-path glue of the backward, one pass over the
+ *   attention backward's dQKV (no GEMM of the chain produces it):
+ *   dYq = RoPE^T(dQKV) (transposed rotation on columns < rope_cols),
+ *   s[i] = (1/d) sum_j dQKV[i,j] QKV[i,j] (equal to (1/d) rowsum(dYq (.) Yq)
+ *   for the unrotated projection Yq: the rotation is orthogonal), and
+ *   dqr = r (.)row dYq. dqkv, qkv [M,N] bf16, r [M], cos/sin [S, head_dim/2]
+ *   -> dqr [M,N] bf16, s [M] fp32. head_dim a multiple of 8. HBM-bound. */
+int coda_rope_bwd_rowdot(int M, int N, const coda_bf16* dqkv, const coda_bf16* qkv, const float* r,
+                         const float* cos_tab, const float* sin_tab, int S, int head_dim, int rope_cols, int d,
+                         coda_bf16* dqr_out, float* s_out, coda_stream_t stream);
+
+/* Descriptor of one period of the chain. Sizes: M tokens, d model width, F
+ * FFN width (Wgu has 2F interleaved gate/up columns), QKV width 3d with RoPE on
+ * columns [0, rope_cols) at position row mod S. All tensors are caller-owned
+ * device memory, row-major, bf16 unless marked fp32. The fused and the unfused
+ * sequences use the same descriptor; where the meaning differs it says so. */
+typedef struct coda_block {
+  int M, d, F;
+  int head_dim, rope_cols, S;
+  float eps;
+  const float* cos_tab; /* [S, head_dim/2] fp32 (coda_rope_tables) */
+  const float* sin_tab;
+  /* forward inputs */
+  const coda_bf16* P;      /* [M,F] activation entering the down projection */
+  const coda_bf16* x;      /* [M,d] residual stream entering the period */
+  const coda_bf16* O;      /* [M,d] attention-core output */
+  const coda_bf16* Wd;     /* [F,d] */
+  const coda_bf16* gamma1; /* [d] */
+  const coda_bf16* Wqkv;   /* [d,3d] */
+  const coda_bf16* Wo;     /* [d,d] */
+  const coda_bf16* gamma2; /* [d] */
+  const coda_bf16* Wgu;    /* [d,2F] */
+  /* written by the forward, read by the backward */
+  coda_bf16* h1;  /* [M,d] residual stream after the RoPE-path GEMM */
+  coda_bf16* h1g; /* [M,d] fused: h1 (.) gamma1; unfused: n1 = RMSNorm(h1) */
+  coda_bf16* h2;  /* [M,d] */
+  coda_bf16* h2g; /* [M,d] fused: h2 (.) gamma2; unfused: n2 */
+  coda_bf16* gu;  /* [M,2F] GU = n2 Wgu (the same tensor on both paths) */
+  float* r1;      /* [M] fp32 inverse RMS of h1 */
+  float* r2;      /* [M] fp32 */
+  /* forward outputs */
+  coda_bf16* qkv; /* [M,3d] rotated QKV */
+  coda_bf16* a;   /* [M,F] SwiGLU output */
+  /* backward inputs */
+  coda_bf16* dqkv;       /* [M,3d] gradient of the rotated QKV; the fused backward only reads it, the
+                            unfused backward rotates it in place (its RoPE backward works in place) */
+  const coda_bf16* gh;   /* [M,d] gradient of the next period's residual output */
+  const coda_bf16* Wdn;  /* [F,d] the next period's down projection */
+  /* backward outputs */
+  coda_bf16* dh1;   /* [M,d] = dL/dx */
+  coda_bf16* dh2;   /* [M,d] */
+  coda_bf16* dO;    /* [M,d] gradient to the attention core */
+  coda_bf16* dWd;   /* [F,d] */
+  coda_bf16* dWqkv; /* [d,3d] */
+  coda_bf16* dWo;   /* [d,d] */
+  coda_bf16* dWgu;  /* [d,2F] */
+  float* dgamma1;   /* [d] fp32 */
+  float* dgamma2;   /* [d] fp32 */
+  /* backward intermediates */
+  coda_bf16* dgur; /* [M,2F] fused: r2 (.)row dGU; unfused: dGU */
+  coda_bf16* dqr;  /* [M,3d] fused: r1 (.)row RoPE^T(dQKV); unused by the unfused backward (may be NULL) */
+  float* s1;       /* [M] fp32 row statistics (fused only) */
+  float* s2;
+  /* scratch: coda_block_workspace_bytes(M, d, F, unfused) bytes, 256-byte aligned */
+  void* workspace;
+} coda_block_t;
+
+/* Scratch bytes the chain needs (partials; and for unfused != 0 also the
+ * intermediates the unfused sequence materialises). 0 for negative sizes. */
+size_t coda_block_workspace_bytes(int M, int d, int F, int unfused);
+
+/* Fused forward: residual + RMS-prep GEMM, coda_rms_reduce,
+ * coda_gemm_rowscale_rope; residual + RMS-prep GEMM, coda_rms_reduce,
+ * coda_gemm_rowscale_swiglu (GU saved). 6 launches. */
+int coda_block_fwd(const coda_block_t* b, coda_stream_t stream);
+
+/* Fused backward (after coda_block_fwd on the same descriptor):
+ * coda_gemm_swiglu_bwd_rowdot, coda_rowdot_reduce, coda_gemm_rmsnorm_bwd_res
+ * (dres = gh), coda_colsum_reduce, dWgu = h2g^T dgur, dO = dh2 Wo^T,
+ * dWo = O^T dh2, coda_rope_bwd_rowdot, coda_gemm_rmsnorm_bwd_res (dres = dh2),
+ * coda_colsum_reduce, dWqkv = h1g^T dqr, dWd = P^T dh1. 13 launches. */
+int coda_block_bwd(const coda_block_t* b, coda_stream_t stream);
+
+/* Unfused forward: plain GEMMs and the stand-alone kernels (add, RMSNorm,
+ * RoPE in place, SwiGLU). 10 launches. */
+int coda_block_fwd_unfused(const coda_block_t* b, coda_stream_t stream);
+
+/* Unfused backward (after coda_block_fwd_unfused): plain GEMMs, SwiGLU
+ * backward, textbook RMSNorm backward, residual adds, RoPE backward in place
+ * on dqkv. 16 launches. */
+int coda_block_bwd_unfused(const coda_block_t* b, coda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,3 +101,56 @@ def test_no_device_is_reported_not_crashed(lib):
     rc = lib.coda_gemm(128, 256, 64, good, 64, 0, good, 256, 0, good, 256, None)
     assert rc in (-2, -3)
     assert lib.coda_last_error()
+
+
+def test_block_descriptor_layout_matches_c(tmp_path):
+    """The ctypes mirror of coda_block_t has the C struct's size and field
+    offsets (compiled with the host C compiler against include/coda.h)."""
+    import shutil
+    import subprocess
+    from gemm_epilogue_transformer_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    names = [f for f, _ in _lib.CodaBlock._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"coda.h\"\nint main(void) {\n"
+                   '  printf("%zu\\n", sizeof(coda_block_t));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(coda_block_t, {n}));\n' for n in names) + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.CodaBlock)
+    assert got[1:] == [getattr(_lib.CodaBlock, n).offset for n in names]
+
+
+def test_block_chain_host_validation(lib):
+    INVALID, UNSUPPORTED = -1, -2
+    good = _p(0x10000)
+    assert lib.coda_block_fwd(None, None) == INVALID
+    from gemm_epilogue_transformer_gb300 import _lib
+    b = _lib.CodaBlock()
+    b.M, b.d, b.F = 64, 100, 64
+    b.workspace = 0x10000
+    assert lib.coda_block_fwd(b, None) == UNSUPPORTED          # d not a multiple of 8
+    b.d = 64
+    b.workspace = 0x10010
+    assert lib.coda_block_bwd(b, None) == INVALID              # workspace not 256-byte aligned
+    # workspace size: partials (fused), plus the unfused intermediates
+    M, d, F = 1000, 256, 384
+    fused = lib.coda_block_workspace_bytes(M, d, F, 0)
+    assert fused >= 4 * (M * 2 + M * 3 + 32 * d)
+    assert lib.coda_block_workspace_bytes(M, d, F, 1) >= fused + 2 * M * (d + F + d)
+    assert lib.coda_block_workspace_bytes(-1, d, F, 0) == 0
+    # composed kernels: granularity and argument checks before any launch
+    assert lib.coda_gemm_rowscale_rope(8, 256, 8, good, good, good, good, good, 16, 48, 128, good, None) == UNSUPPORTED
+    assert lib.coda_gemm_rowscale_rope(8, 256, 8, good, good, None, good, good, 16, 64, 128, good, None) == INVALID
+    assert lib.coda_gemm_rowscale_swiglu(8, 12, 8, good, good, good, good, None, None) == UNSUPPORTED
+    assert lib.coda_gemm_swiglu_bwd_rowdot(8, 16, 8, good, good, good, None, good, good, None) == INVALID
+    assert lib.coda_gemm_rmsnorm_bwd_res(8, 16, 8, good, good, good, good, good, good, None, good, good,
+                                         None) == INVALID
+    assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 12, 48, 32, good, good,
+                                    None) == UNSUPPORTED
+    assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 16, 40, 32, good, good,
+                                    None) == INVALID
+    assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 16, 48, 0, good, good, None) == INVALID
