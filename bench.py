@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite")
     ap.add_argument("--only", default=None,
                     help="with --suite: run one workload (rmsnorm_chain_tiny, rmsnorm_chain_8192, rope_qkv_4096, "
-                         "swiglu_up_4096, lm_head_ce_8192)")
+                         "swiglu_up_4096, lm_head_ce_8192, block_d2048, block_d4096, block_d8192)")
     return ap.parse_args()
 
 
@@ -490,6 +490,9 @@ def suite(a):
         swiglu_suite(G, gen, d, dev, report)
     if want("lm_head_ce_8192"):
         ce_suite(G, gen, d, dev, report)
+    for dm in sorted(gen.BLOCK_SIZES):
+        if want(f"block_d{dm}"):
+            block_suite(G, gen, dev, report, dm)
     status = G.coda_device_status(clear=True)
     print(json.dumps({"suite": "done", "device_status": status}), flush=True)
     return 0 if status == 0 else 1
@@ -555,6 +558,41 @@ def ce_suite(G, gen, d, dev, report):
            lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
            lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
            "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel")
+
+
+def block_suite(G, gen, dev, report, dm):
+    """One period of the block-level chain (RoPE-path and SwiGLU-path
+    GEMM-residual-RMSNorm-GEMM structures) at 16K tokens, forward and forward +
+    backward, fused sequence vs unfused sequence. Inputs are drawn on the
+    device (seeded torch generator) with the distributions of
+    coda_inputs.block_problem: a host-side draw of the 70B-scale tensors would
+    take longer than the timing itself."""
+    import torch
+    c = gen.WORKLOADS[f"block_d{dm}"]
+    M, d, F, hd, rc, S = c["M"], c["d"], c["F"], c["head_dim"], c["rope_cols"], c["S"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+
+    def normal(shape, std=1.0, mean=0.0):
+        t = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        return (t * std + mean).to(torch.bfloat16)
+
+    t = dict(P=normal((M, F)), Wd=normal((F, d), F ** -0.5), x=normal((M, d)), gamma1=normal((d,), 0.1, 1.0),
+             Wqkv=normal((d, 3 * d), d ** -0.5), O=normal((M, d)), Wo=normal((d, d), d ** -0.5),
+             gamma2=normal((d,), 0.1, 1.0), Wgu=normal((d, 2 * F), d ** -0.5), dQKV=normal((M, 3 * d)),
+             gh=normal((M, d)), Wdn=normal((F, d), F ** -0.5))
+    cos, sin = G.coda_rope_tables(S, hd, c["theta"], device=dev)
+    fl_fwd = 2.0 * M * d * (3 * F + 4 * d)
+    fused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"])
+    unfused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"], unfused=True)
+    name = f"block_d{dm}"
+    report(name, "fwd", fl_fwd, fused.fwd, unfused.fwd_unfused, "6 fused launches vs 10 unfused")
+    fused.fwd()
+    unfused.fwd_unfused()
+    report(name, "fwd_bwd", 3 * fl_fwd, lambda: fused.fwd().bwd(), lambda: unfused.fwd_unfused().bwd_unfused(),
+           "19 fused launches vs 26 unfused")
+    del t, fused, unfused
+    torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":

@@ -79,7 +79,7 @@ constexpr int BSEG = 128;  // epilogue segment: columns per partial-statistics b
 
 struct GemmShape {
   int M, N, K;
-  int a_mn, b_mn;
+  int a_mn, b_mn;  // 0: K-major; 1: MN-major, 64-wide 2-D boxes; 2: MN-major, one 3-D box per stage
   int m_blocks, n_blocks, k_blocks, num_tiles, group_m;
   // Work items: the first full_items are whole tiles in raster order; each of
   // the remaining tiles (a partial last wave) is split into two 128-column
@@ -332,10 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = m_blk * C::kTileM + static_cast<int>(rank) * BM;
         const int bcols = ncols / kCG;  // B columns this CTA loads
         const int nb0 = n0 + static_cast<int>(rank) * bcols;
-        // N-major B arrives in 64-column boxes; K-major B as one box of
-        // kBLoad rows (a half tile reads past its columns: harmless extra bytes)
-        const int nbox = p.b_mn ? bcols / 64 : 0;
-        const uint32_t tx = kCG * (C::kABytes + (p.b_mn ? static_cast<uint32_t>(bcols * BK * 2) : C::kBBytes));
+        // N-major B arrives in 64-column boxes (b_mn 1) or as one 3-D box of
+        // kBLoad columns (b_mn 2); K-major B as one box of kBLoad rows (a half
+        // tile reads past its columns: harmless extra bytes)
+        const int nbox = p.b_mn == 1 ? bcols / 64 : 0;
+        const uint32_t tx = kCG * (C::kABytes + (p.b_mn == 1 ? static_cast<uint32_t>(bcols * BK * 2) : C::kBBytes));
         // The k-loop is the kernel's critical path: keep it to the wait, the
         // expected-bytes arrive and the copies.
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -355,13 +356,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tma_load_2d(dst, m, fb_target, x, y);
           };
-          if (p.a_mn) {
+          auto load3 = [&](uint32_t dst, const CUtensorMap* m, int y, int z) {
+            if constexpr (kCG == 2)
+              tma_load_3d_pair(dst, m, fb_target, 0, y, z);
+            else
+              tma_load_3d(dst, m, fb_target, 0, y, z);
+          };
+          if (p.a_mn == 2) {
+            load3(a_dst, &tmA, k0, m0 >> 6);
+          } else if (p.a_mn) {
             load(a_dst, &tmA, m0, k0);
             load(a_dst + 8192, &tmA, m0 + 64, k0);
           } else {
             load(a_dst, &tmA, k0, m0);
           }
-          if (p.b_mn) {
+          if (p.b_mn == 2) {
+            load3(b_dst, &tmB, k0, nb0 >> 6);
+          } else if (p.b_mn) {
 #pragma unroll
             for (int j = 0; j < C::kBLoad / 64; ++j)
               if (j < nbox) load(b_dst + j * 8192, &tmB, nb0 + 64 * j, k0);
@@ -389,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc_full = idesc_bf16_f32(C::kTileM, BN, p.a_mn, p.b_mn);
-      const uint32_t idesc_half = idesc_bf16_f32(C::kTileM, BSEG, p.a_mn, p.b_mn);
+      const int amn = p.a_mn != 0, bmn = p.b_mn != 0;
+      const uint32_t idesc_full = idesc_bf16_f32(C::kTileM, BN, amn, bmn);
+      const uint32_t idesc_half = idesc_bf16_f32(C::kTileM, BSEG, amn, bmn);
       // Operand descriptors. K-major: 128B rows, 8-row groups 1024B apart,
       // K advances 32B (16 bf16) inside the swizzle atom. MN-major: 64-element
       // MN chunks 8192B apart (LBO), 8-row K groups 1024B apart (SBO), K

@@ -45,13 +45,24 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
   int rc;
+  // An MN-major operand whose MN extent is a multiple of 64 is read with one
+  // 3-D box per stage (mode 2) instead of one 2-D box per 64 columns (mode 1).
+  if (a_mn && M % 64 == 0) a_mn = 2;
+  if (b_mn && N % 64 == 0) b_mn = 2;
   if (K > 0) {
-    rc = a_mn ? make_map_bf16(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-              : make_map_bf16(&tA, A, K, M, static_cast<uint64_t>(lda) * 2u, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (a_mn == 2)
+      rc = make_map_bf16_mn3d(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, BM / 64);
+    else if (a_mn)
+      rc = make_map_bf16(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      rc = make_map_bf16(&tA, A, K, M, static_cast<uint64_t>(lda) * 2u, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
-    rc = b_mn ? make_map_bf16(&tB, B, N, K, static_cast<uint64_t>(ldb) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
-              : make_map_bf16(&tB, B, K, N, static_cast<uint64_t>(ldb) * 2u, 64, C::kBLoad,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
+    if (b_mn == 2)
+      rc = make_map_bf16_mn3d(&tB, B, N, K, static_cast<uint64_t>(ldb) * 2u, C::kBLoad / 64);
+    else if (b_mn)
+      rc = make_map_bf16(&tB, B, N, K, static_cast<uint64_t>(ldb) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      rc = make_map_bf16(&tB, B, K, N, static_cast<uint64_t>(ldb) * 2u, 64, C::kBLoad, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   auto kernel = &gemm_epilogue_kernel<Epi, kCG>;

@@ -47,6 +47,10 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 // `row_bytes`, box {box_inner, box_outer}, the given swizzle.
 int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+// A row-major [k, mn] bf16 array read MN-major as boxes of `chunks` 64 x 64
+// atoms (3-D map {64, k, mn/64}); mn a multiple of 64.
+int make_map_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t mn, uint64_t k, uint64_t row_bytes,
+                       uint32_t chunks);
 // The same for an fp32 array.
 int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);

@@ -117,6 +117,32 @@ static int make_map(CUtensorMapDataType dt, CUtensorMap* m, const void* base, ui
   return CODA_OK;
 }
 
+// A row-major [k, mn] bf16 operand used MN-major, viewed as 3-D {64, k, mn/64}
+// (element in a 64-wide chunk, row, chunk) with strides {row_bytes, 128 B}, so
+// that one box of {64, 64, chunks} lands in shared memory as `chunks`
+// consecutive 128B-swizzled 64 x 64 atoms (8 KiB each): the layout of
+// `chunks` separate 2-D boxes, in one copy. mn must be a multiple of 64 (a
+// partial last chunk would read the next row instead of zeros).
+int make_map_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t mn, uint64_t k, uint64_t row_bytes,
+                       uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CODA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  if (mn % 64 != 0) return fail(CODA_ERR_INVALID, "3-D operand map needs a multiple of 64 columns (got %llu)",
+                                (unsigned long long)mn);
+  cuuint64_t dims[3] = {64, k, mn / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(CODA_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d): mn %llu k %llu stride %llu chunks %u",
+                static_cast<int>(r), (unsigned long long)mn, (unsigned long long)k, (unsigned long long)row_bytes,
+                chunks);
+  return CODA_OK;
+}
+
 int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   return make_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m, base, inner, outer, row_bytes, box_inner, box_outer, sw);

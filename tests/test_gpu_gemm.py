@@ -18,6 +18,7 @@ SHAPES = [
     (640, 1024, 2048),  # 5 x 4 tiles, 32 k-blocks
     (2560, 4096, 128),  # 320 tiles: two or three tiles per persistent CTA
     (4096, 3072, 264),  # 384 tiles, ragged K
+    (200, 264, 72),     # transposed operands with M, N not multiples of 64 (one 2-D box per 64 columns)
 ]
 
 
@@ -70,3 +71,23 @@ def test_gemm_leading_dims(coda, cta_group):
     coda.coda_gemm(dA[:, :K], dB[:K, :N], out=out[:, :N])
     assert_bf16(f64(out[:, :N]), O.matmul(O.bf16(A)[:, :K], O.bf16(B)[:K, :N]), "gemm strided")
     assert float(out[:, N:].float().abs().max()) == 0.0, "wrote past the logical columns"
+
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (1, 1)])
+def test_gemm_leading_dimensions(coda, cta_group, ta, tb):
+    """Operands that are column slices of wider arrays (lda, ldb above the row
+    length), for the 3-D (multiple of 64) and the 2-D operand maps."""
+    M, N, K = 384, 320, 200
+    A, B = _operands(M, N, K, ta, tb, seed=11 + ta + 2 * tb)
+    pad = 72
+    Aw = np.zeros((A.shape[0], A.shape[1] + pad), np.uint16)
+    Aw[:, :A.shape[1]] = A
+    Bw = np.zeros((B.shape[0], B.shape[1] + pad), np.uint16)
+    Bw[:, :B.shape[1]] = B
+    dA = dev_bf16(Aw)[:, :A.shape[1]]
+    dB = dev_bf16(Bw)[:, :B.shape[1]]
+    assert dA.stride(0) == A.shape[1] + pad
+    C = coda.coda_gemm(dA, dB, transA=bool(ta), transB=bool(tb))
+    a = O.bf16(A).T if ta else O.bf16(A)
+    b = O.bf16(B).T if tb else O.bf16(B)
+    assert_bf16(f64(C), O.matmul(a, b), f"strided gemm ta={ta} tb={tb}")
