@@ -101,12 +101,38 @@ __global__ void mean_kernel(int M, const float* __restrict__ v, float* __restric
   }
 }
 
-// dgamma[j] = sum_b pdg[b, j]
-__global__ void colsum_kernel(int rows, int d, const float* __restrict__ pdg, float* __restrict__ out) {
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < d; j += gridDim.x * blockDim.x) {
+// dgamma[j] = sum_b pdg[b, j]. A block owns a strip of 32 columns (one
+// coalesced 128-byte segment per row); its 16 warps take interleaved rows,
+// 8 independent loads in flight per lane, and combine their sums in shared
+// memory in a fixed order (deterministic).
+constexpr int kColsumWarps = 16;
+__global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(int rows, int d, const float* __restrict__ pdg,
+                                                                   float* __restrict__ out) {
+  __shared__ float sh[kColsumWarps][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int j0 = blockIdx.x * 32; j0 < d; j0 += gridDim.x * 32) {
+    const int j = j0 + lane;
     float s = 0.f;
-    for (int b = 0; b < rows; ++b) s += pdg[static_cast<long>(b) * d + j];
-    out[j] = s;
+    if (j < d) {
+      int b = w;
+      for (; b + 7 * kColsumWarps < rows; b += 8 * kColsumWarps) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(pdg + static_cast<long>(b + u * kColsumWarps) * d + j);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += v[u];
+      }
+      for (; b < rows; b += kColsumWarps) s += __ldg(pdg + static_cast<long>(b) * d + j);
+    }
+    sh[w][lane] = s;
+    __syncthreads();
+    if (w == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int q = 0; q < kColsumWarps; ++q) t += sh[q][lane];
+      if (j < d) out[j] = t;
+    }
+    __syncthreads();
   }
 }
 
@@ -202,7 +228,9 @@ int coda_colsum_reduce(int rows, int d, const float* pdg, float* dgamma_out, cod
   if (rows > 0) CODA_REQ_PTR4(pdg);
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
-  colsum_kernel<<<(d + 255) / 256, 256, 0, as_stream(stream)>>>(rows, d, pdg, dgamma_out);
+  const int strips = (d + 31) / 32;
+  const int grid = strips < di->sm_count * 4 ? strips : di->sm_count * 4;
+  colsum_kernel<<<grid, kColsumWarps * 32, 0, as_stream(stream)>>>(rows, d, pdg, dgamma_out);
   return launched(fn);
 }
 
