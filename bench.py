@@ -409,23 +409,27 @@ def suite(a):
     def d(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    def t_ms(fn):
-        for _ in range(3):
-            fn()
-        ts = []
-        for _ in range(a.reps):
-            flush.zero_()
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            fn()
-            e.record(stream)
-            e.synchronize()
-            ts.append(s.elapsed_time(e))
-        return float(np.median(ts)), float(np.min(ts))
+    def once(fn):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        return s.elapsed_time(e)
 
     def report(workload, op, flops, fused, unfused, launches):
-        fm, fmin = t_ms(fused)
-        um, umin = t_ms(unfused)
+        # fused and unfused repetitions alternate, so clock and power drift over
+        # the run affect both columns alike
+        for _ in range(3):
+            fused()
+            unfused()
+        tf, tu = [], []
+        for _ in range(a.reps):
+            tf.append(once(fused))
+            tu.append(once(unfused))
+        fm, fmin = float(np.median(tf)), float(np.min(tf))
+        um, umin = float(np.median(tu)), float(np.min(tu))
         line = {"suite": workload, "op": op, "fused_ms": fm, "fused_min_ms": fmin, "unfused_ms": um,
                 "unfused_min_ms": umin, "speedup_vs_unfused": um / fm,
                 "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None,
