@@ -528,6 +528,11 @@ class CodaBlock:
     def fwd(self, stream=None):
         return self._run("coda_block_fwd", stream)
 
+    def fwd_noalloc(self, stream=None):
+        """The fused forward with the library's static scratch instead of the
+        workspace (coda_block_fwd_noalloc); calls must not overlap on the GPU."""
+        return self._run("coda_block_fwd_noalloc", stream)
+
     def bwd(self, stream=None):
         return self._run("coda_block_bwd", stream)
 

@@ -77,6 +77,7 @@ SIGNATURES = {
     "coda_rope_bwd_rowdot": (I, [I, I, P, P, P, P, P, I, I, I, I, P, P, P]),
     "coda_block_workspace_bytes": (c_size_t, [I, I, I, I]),
     "coda_block_fwd": (I, [BLK, P]),
+    "coda_block_fwd_noalloc": (I, [BLK, P]),
     "coda_block_bwd": (I, [BLK, P]),
     "coda_block_fwd_unfused": (I, [BLK, P]),
     "coda_block_bwd_unfused": (I, [BLK, P]),

@@ -13,6 +13,8 @@
 // over dQKV and the saved QKV.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "host.h"
 
 using namespace coda;
@@ -143,6 +145,36 @@ int check_block(const char* fn, const coda_block_t* b) {
   return CODA_OK;
 }
 
+// Scratch of coda_block_fwd_noalloc: the forward's only scratch, the
+// per-(row, 128-column block) sum-of-squares partials, in a file-scope device
+// array instead of the caller's workspace. One array per device (the module
+// is loaded per context), shared by every call on that device.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB: M * ceil(d/128) fp32 partials
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (with that device current) and cached; nullptr after fail().
+void* noalloc_scratch() {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    fail(CODA_ERR_CUDA, "coda_block_fwd_noalloc: no current device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      fail_cuda(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress(noalloc scratch)");
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 #define CODA_TRY(call)        \
   do {                        \
     const int rc_ = (call);   \
@@ -209,6 +241,24 @@ int coda_block_fwd(const coda_block_t* b, coda_stream_t stream) {
   CODA_TRY(coda_rms_reduce(M, nbd, d, w.psq, b->eps, b->r2, stream));
   CODA_TRY(coda_gemm_rowscale_swiglu(M, F, d, b->h2g, b->Wgu, b->r2, b->a, b->gu, stream));
   return CODA_OK;
+}
+
+int coda_block_fwd_noalloc(const coda_block_t* b, coda_stream_t stream) {
+  const char* fn = "coda_block_fwd_noalloc";
+  CODA_REQUIRE(b != nullptr, CODA_ERR_INVALID, "%s: null block descriptor", fn);
+  CODA_REQUIRE(b->M >= 0 && b->d >= 0 && b->F >= 0, CODA_ERR_INVALID, "%s: negative size", fn);
+  const size_t need = static_cast<size_t>(b->M) * static_cast<size_t>((b->d + 127) / 128) * sizeof(float);
+  CODA_REQUIRE(need <= kNoAllocScratchBytes, CODA_ERR_UNSUPPORTED,
+               "%s: M * ceil(d/128) * 4 = %zu bytes of partials exceed the %zu-byte static scratch", fn, need,
+               kNoAllocScratchBytes);
+  if (b->M == 0) return CODA_OK;
+  void* scratch = noalloc_scratch();
+  if (!scratch) return CODA_ERR_CUDA;
+  // the same launch sequence as coda_block_fwd, with the static array as its workspace (the
+  // forward touches only the partials, which the workspace layout places first)
+  coda_block_t c = *b;
+  c.workspace = scratch;
+  return coda_block_fwd(&c, stream);
 }
 
 int coda_block_bwd(const coda_block_t* b, coda_stream_t stream) {

@@ -402,6 +402,18 @@ size_t coda_block_workspace_bytes(int M, int d, int F, int unfused);
  * coda_gemm_rowscale_swiglu (GU saved). 6 launches. */
 int coda_block_fwd(const coda_block_t* b, coda_stream_t stream);
 
+/* coda_block_fwd_noalloc: the fused forward for callers that cannot allocate
+ * device memory. It has no counterpart on the pages (a deployment convenience
+ * of this library). It runs the launch sequence of coda_block_fwd but ignores
+ * b->workspace: the forward's only scratch, the sum-of-squares partials
+ * (M * ceil(d/128) fp32 values), lives in a 4 MiB file-scope device array of
+ * the library, one per device. Sizes with M * ceil(d/128) * 4 > 4 MiB return
+ * CODA_ERR_UNSUPPORTED (M = 16384 fits up to d = 8192). Two calls whose
+ * kernels can overlap on the GPU (calls on different streams, or from threads
+ * whose streams are not ordered) race on that array and give undefined
+ * results; calls on one stream run in order and are safe. Allocates nothing. */
+int coda_block_fwd_noalloc(const coda_block_t* b, coda_stream_t stream);
+
 /* Fused backward (after coda_block_fwd on the same descriptor):
  * coda_gemm_swiglu_bwd_rowdot, coda_rowdot_reduce, coda_gemm_rmsnorm_bwd_res
  * (dres = gh), coda_colsum_reduce, dWgu = h2g^T dgur, dO = dh2 Wo^T,

@@ -1,0 +1,55 @@
+"""The block-chain forward without a caller workspace (coda_block_fwd_noalloc):
+its sum-of-squares partials live in the library's static device array. Two
+calls in a row on one stream must both give the workspace variant's bits and
+match the float64 oracle; a size past the array's limit is refused before any
+launch."""
+import numpy as np
+import pytest
+
+import coda_inputs as gen
+import oracle as O
+from _util import assert_stat, dev_bf16, f64
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+THETA = 10000.0
+
+
+def test_block_fwd_noalloc_twice(coda):
+    import torch
+    M, d, F, hd, S = 200, 256, 384, 64, 128
+    rc = 2 * d
+    p = gen.block_problem(M, d, F, seed=21, with_bwd=False)
+    t = {k: dev_bf16(v) for k, v in p.items()}
+    cos, sin = coda.coda_rope_tables(S, hd, THETA)
+    ref_blk = coda.CodaBlock(t, hd, rc, cos, sin, EPS).fwd()
+    blk = coda.CodaBlock(t, hd, rc, cos, sin, EPS)
+    outs = []
+    for _ in range(2):
+        for k in ("h1", "h1g", "h2", "h2g", "gu", "qkv", "a", "r1", "r2"):
+            getattr(blk, k).fill_(float("nan"))
+        blk.fwd_noalloc()
+        torch.cuda.synchronize()
+        outs.append({k: getattr(blk, k).clone() for k in ("h1", "h2", "gu", "qkv", "a", "r1", "r2")})
+    for k in outs[0]:
+        assert torch.equal(outs[0][k], outs[1][k]), f"{k}: the two calls differ"
+        assert torch.equal(outs[0][k], getattr(ref_blk, k)), f"{k}: differs from the workspace variant"
+    b = {k: O.bf16(v) for k, v in p.items()}
+    pos = np.arange(M) % S
+    f = O.block_fwd(b["P"], b["Wd"], b["x"], b["gamma1"], b["Wqkv"], b["O"], b["Wo"], b["gamma2"], b["Wgu"], pos,
+                    hd, THETA, rc, EPS)
+    assert_stat(f64(blk.r1), O.rms_scale(O.res_rmsprep(b["P"], b["Wd"], b["x"], b["gamma1"])["h1"], EPS), "r1")
+    for name in ("QKV", "A"):
+        got = f64(blk.qkv if name == "QKV" else blk.a)
+        err = np.linalg.norm(got - f[name]) / np.linalg.norm(f[name])
+        assert err <= 1e-2, f"{name}: rel Frobenius {err:.3e} against the float64 chain"
+    assert coda.coda_device_status(clear=True) == 0
+
+
+def test_block_fwd_noalloc_limit(coda):
+    from gemm_epilogue_transformer_gb300 import _lib
+    b = _lib.CodaBlock()
+    b.M, b.d, b.F = 1 << 20, 1024, 1024   # 2^20 rows x 8 blocks x 4 B = 32 MiB of partials
+    assert coda.lib().coda_block_fwd_noalloc(b, None) == -2  # CODA_ERR_UNSUPPORTED, nothing launched
+    assert b"static scratch" in coda.lib().coda_last_error()
