@@ -20,7 +20,6 @@ on a bounded sample of the same workload instead. Multi-GPU: replicas only
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -165,10 +164,16 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+# The sources that define the fused RoPE kernel and its launch: the committed
+# ncu traffic applies while these are unchanged.
+ROPE_KERNEL_SOURCES = ("ptx.cuh", "gemm_core.cuh", "epilogues.cuh", "gemm_launch.cuh", "host.h", "gemm_fwd.cu",
+                       "runtime.cu")
+
+
 def kernel_src_hash():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "gemm_epilogue_transformer_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in ROPE_KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "gemm_epilogue_transformer_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -238,15 +243,16 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def fused_step(x, w, a_, b_, ev=None):
+    def fused_step(x, w, a_, b_, ev=None, outs=None):
+        o, p_, dx, dw = outs if outs is not None else (out, dP, dX, dW)
         if ev is not None:
             ev[0].record(stream)
-        G.coda_gemm_rope(x, w, cos, sin, hd, rc, out=out)
+        G.coda_gemm_rope(x, w, cos, sin, hd, rc, out=o)
         if ev is not None:
             ev[1].record(stream)
-        G.coda_gemm_rope_bwd(a_, b_, cos, sin, hd, rc, out=dP)
-        G.coda_gemm(dP, w, transB=True, out=dX)
-        G.coda_gemm(x, dP, transA=True, out=dW)
+        G.coda_gemm_rope_bwd(a_, b_, cos, sin, hd, rc, out=p_)
+        G.coda_gemm(p_, w, transB=True, out=dx)
+        G.coda_gemm(x, p_, transA=True, out=dw)
 
     def unfused_step():
         G.coda_gemm(X, W, out=out)
@@ -287,37 +293,82 @@ def main():
     ms_fused, ms_rope = timed(lambda ev: fused_step(X, W, A, B, ev), a.steps, kernel_events=True)
     ms_unfused, _ = timed(lambda ev: unfused_step(), a.steps)
 
-    # end to end through the public API: pinned host inputs -> device, the step,
-    # results back to pinned host memory, all inside each timed step
-    h_out = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    h_dX = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
-    h_dW = torch.empty((K, N), dtype=torch.bfloat16).pin_memory()
-    dXin = torch.empty_like(X)
-    dWin = torch.empty_like(W)
-    dAin = torch.empty_like(A)
-    dBin = torch.empty_like(B)
+    # End to end through the public API: every step copies its four inputs from
+    # pinned host memory to the device, runs the step, and copies its three
+    # results back to pinned host memory. Serial: all on the compute stream.
+    # Pipelined (the reported e2e): host-to-device copies on one copy stream,
+    # device-to-host copies on another, double-buffered device inputs and
+    # outputs and two sets of host result buffers, so step i's copies overlap
+    # the neighbouring steps' compute and each other; every step still moves
+    # all of its bytes inside the timed region.
+    names_in = ("X", "W", "A", "B")
+    d_in = [{k: torch.empty_like(host[k], device=dev) for k in names_in} for _ in range(2)]
+    d_out = [(torch.empty_like(out), torch.empty_like(dP), torch.empty_like(dX), torch.empty_like(dW))
+             for _ in range(2)]
+    h_res = [(torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+              torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
+              torch.empty((K, N), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
 
-    def e2e_step(_ev):
-        dXin.copy_(host["X"], non_blocking=True)
-        dWin.copy_(host["W"], non_blocking=True)
-        dAin.copy_(host["A"], non_blocking=True)
-        dBin.copy_(host["B"], non_blocking=True)
-        fused_step(dXin, dWin, dAin, dBin)
-        h_out.copy_(out, non_blocking=True)
-        h_dX.copy_(dX, non_blocking=True)
-        h_dW.copy_(dW, non_blocking=True)
+    def e2e_serial_step(_ev):
+        di, do, hr = d_in[0], d_out[0], h_res[0]
+        for k in names_in:
+            di[k].copy_(host[k], non_blocking=True)
+        fused_step(di["X"], di["W"], di["A"], di["B"], outs=do)
+        hr[0].copy_(do[0], non_blocking=True)
+        hr[1].copy_(do[2], non_blocking=True)
+        hr[2].copy_(do[3], non_blocking=True)
+
+    s_h2d = torch.cuda.Stream(dev)
+    s_d2h = torch.cuda.Stream(dev)
+
+    def e2e_pipelined(steps):
+        ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+        in_ready, in_free = [ev(), ev()], [ev(), ev()]
+        out_ready, out_free = [ev(), ev()], [ev(), ev()]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        t0.record(stream)
+        for j in range(2):
+            in_free[j].record(stream)
+            out_free[j].record(stream)
+        for i in range(steps):
+            j = i % 2
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(in_free[j])
+                for k in names_in:
+                    d_in[j][k].copy_(host[k], non_blocking=True)
+                in_ready[j].record(s_h2d)
+            stream.wait_event(in_ready[j])
+            stream.wait_event(out_free[j])
+            fused_step(d_in[j]["X"], d_in[j]["W"], d_in[j]["A"], d_in[j]["B"], outs=d_out[j])
+            in_free[j].record(stream)
+            out_ready[j].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(out_ready[j])
+                h_res[j][0].copy_(d_out[j][0], non_blocking=True)
+                h_res[j][1].copy_(d_out[j][2], non_blocking=True)
+                h_res[j][2].copy_(d_out[j][3], non_blocking=True)
+                out_free[j].record(s_d2h)
+        for j in range(2):
+            stream.wait_event(out_free[j])
+        t1.record(stream)
+        barrier()
+        return t0.elapsed_time(t1) / steps
 
     e2e_steps = max(3, min(a.steps, 50))
     for _ in range(2):
-        e2e_step(None)
-    ms_e2e, _ = timed(e2e_step, e2e_steps)
+        e2e_serial_step(None)
+    ms_e2e_serial, _ = timed(e2e_serial_step, e2e_steps)
+    e2e_pipelined(3)
+    ms_e2e = e2e_pipelined(e2e_steps)
     clk = clocks.stop()
     status = G.coda_device_status(clear=True)
     h2d = sum(host[k].numel() * 2 for k in ("X", "W", "A", "B"))
     d2h = (M * N + M * K + K * N) * 2
 
     if dist:
-        ms_fused, ms_unfused, ms_e2e, ms_rope = max_over_ranks([ms_fused, ms_unfused, ms_e2e, ms_rope], dist, dev)
+        ms_fused, ms_unfused, ms_e2e, ms_e2e_serial, ms_rope = max_over_ranks(
+            [ms_fused, ms_unfused, ms_e2e, ms_e2e_serial, ms_rope], dist, dev)
 
     if rank != 0:
         if dist:
@@ -346,7 +397,10 @@ def main():
         "pct_bf16_peak": 100.0 * (FLOPS_PER_STEP / (ms_fused * 1e-3) / 1e12) / peak_tf,
         "clocks": clk,
         "e2e": {"value": world * FLOPS_PER_STEP / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "pipeline": "copy streams overlap compute, double-buffered",
+                "serial_ms_per_step": ms_e2e_serial,
+                "serial_value": world * FLOPS_PER_STEP / (ms_e2e_serial * 1e-3) / 1e12},
         "gpu_launches": 4 * a.steps,
         "roofline": {"kernel": "coda_gemm_rope (gemm_epilogue_kernel<EpiRope<1>>)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
