@@ -110,3 +110,69 @@ def test_lm_head_ce_8192(coda):
     sure = (top2[:, 1] - top2[:, 0]) > 1e-5 * np.sqrt(K) * np.max(np.abs(L), axis=1) + 1e-6
     assert np.array_equal(am.cpu().numpy()[rows][sure], ref["argmax"][sure])
     assert_bf16(f64(dl[rows]), O.ce_bwd(L, p["labels"][rows], f64(lse[rows]), 1.0 / M), "dl rows")
+
+
+def test_block_chain_d4096(coda):
+    """One period of the block-level chain at 16384 tokens, d = 4096, F = 14336:
+    every kernel of the fused forward and backward on sampled rows (row-local
+    outputs) or sampled columns (weight and gamma gradients), against the
+    float64 oracle evaluated on the tensors that kernel consumed."""
+    c = gen.WORKLOADS["block_d4096"]
+    M, d, F, hd, rc, S = c["M"], c["d"], c["F"], c["head_dim"], c["rope_cols"], c["S"]
+    p = gen.block_problem(M, d, F, seed=0)
+    t = {k: dev_bf16(v) for k, v in p.items()}
+    cos, sin = coda.coda_rope_tables(S, hd, c["theta"])
+    blk = coda.CodaBlock(t, hd, rc, cos, sin, c["eps"]).fwd().bwd()
+    b = {k: O.bf16(v) for k, v in p.items()}
+    rows = _rows(M, n=24)
+    pos = rows % S
+    g = lambda x, r=rows: f64(x[r])  # noqa: E731
+
+    # forward, row-local
+    a1 = O.res_rmsprep(b["P"][rows], b["Wd"], b["x"][rows], b["gamma1"])
+    assert_bf16(g(blk.h1), a1["h1"], "h1 rows")
+    assert_bf16(g(blk.h1g), a1["h2"], "h1g rows")
+    assert_stat(g(blk.r1), O.rms_scale(a1["h1"], c["eps"]), "r1 rows")
+    assert_bf16(g(blk.qkv), O.gemm_rowscale_rope(g(blk.h1g), b["Wqkv"], g(blk.r1), pos, hd, c["theta"], rc),
+                "QKV rows")
+    a2 = O.res_rmsprep(b["O"][rows], b["Wo"], g(blk.h1), b["gamma2"])
+    assert_bf16(g(blk.h2), a2["h1"], "h2 rows")
+    assert_stat(g(blk.r2), O.rms_scale(a2["h1"], c["eps"]), "r2 rows")
+    sw = O.gemm_rowscale_swiglu(g(blk.h2g), b["Wgu"], g(blk.r2))
+    assert_bf16(g(blk.gu), sw["GU"], "GU rows")
+    assert_bf16(g(blk.a), sw["A"], "A rows")
+
+    # backward, row-local
+    b1 = O.gemm_swiglu_bwd_rowdot(b["gh"][rows], b["Wdn"], g(blk.gu), g(blk.r2), d)
+    assert_bf16(g(blk.dgur), b1["dGUr"], "dGUr rows")
+    assert_stat(g(blk.s2), b1["s"], "s2 rows")
+    b3 = O.gemm_rmsnorm_bwd_res(g(blk.dgur), b["Wgu"], g(blk.h2), b["gamma2"], g(blk.r2), g(blk.s2), b["gh"][rows])
+    assert_bf16(g(blk.dh2), b3["dh"], "dh2 rows")
+    assert_bf16(g(blk.dO), O.matmul(g(blk.dh2), b["Wo"].T), "dO rows")
+    gl = O.rope_bwd_rowdot(b["dQKV"][rows], g(blk.qkv), g(blk.r1), pos, hd, c["theta"], rc, d)
+    assert_bf16(g(blk.dqr), gl["dYqr"], "dYqr rows")
+    assert_stat(g(blk.s1), gl["s"], "s1 rows")
+    b10 = O.gemm_rmsnorm_bwd_res(g(blk.dqr), b["Wqkv"], g(blk.h1), b["gamma1"], g(blk.r1), g(blk.s1), g(blk.dh2))
+    assert_bf16(g(blk.dh1), b10["dh"], "dh1 rows")
+
+    # column outputs: sums over all 16384 rows, in row chunks
+    cols = _rows(d, n=16, seed=3)
+    cols_gu = _rows(2 * F, n=16, seed=4)
+    cols_qkv = _rows(3 * d, n=16, seed=5)
+    acc = {k: 0.0 for k in ("dg2", "dg1", "dWgu", "dWo", "dWqkv", "dWd")}
+    for r0 in range(0, M, 2048):
+        rr = np.arange(r0, min(M, r0 + 2048))
+        dgur, dqr, dh1, dh2 = g(blk.dgur, rr), g(blk.dqr, rr), g(blk.dh1, rr), g(blk.dh2, rr)
+        acc["dg2"] = acc["dg2"] + np.sum(O.matmul(dgur, b["Wgu"][cols].T) * g(blk.h2, rr)[:, cols], axis=0)
+        acc["dg1"] = acc["dg1"] + np.sum(O.matmul(dqr, b["Wqkv"][cols].T) * g(blk.h1, rr)[:, cols], axis=0)
+        acc["dWgu"] = acc["dWgu"] + O.matmul(g(blk.h2g, rr).T, dgur[:, cols_gu])
+        acc["dWo"] = acc["dWo"] + O.matmul(b["O"][rr].T, dh2[:, cols])
+        acc["dWqkv"] = acc["dWqkv"] + O.matmul(g(blk.h1g, rr).T, dqr[:, cols_qkv])
+        acc["dWd"] = acc["dWd"] + O.matmul(b["P"][rr].T, dh1[:, cols])
+    assert_stat(f64(blk.dgamma2[cols]), acc["dg2"], "dgamma2 columns")
+    assert_stat(f64(blk.dgamma1[cols]), acc["dg1"], "dgamma1 columns")
+    assert_bf16(f64(blk.dWgu[:, cols_gu]), acc["dWgu"], "dWgu columns")
+    assert_bf16(f64(blk.dWo[:, cols]), acc["dWo"], "dWo columns")
+    assert_bf16(f64(blk.dWqkv[:, cols_qkv]), acc["dWqkv"], "dWqkv columns")
+    assert_bf16(f64(blk.dWd[:, cols]), acc["dWd"], "dWd columns")
+    assert coda.coda_device_status(clear=True) == 0
