@@ -27,6 +27,9 @@ import numpy as np
 __all__ = [
     "f32_to_bf16_bits",
     "normal_bf16",
+    "f32_to_e4m3_bits",
+    "normal_e4m3",
+    "fp8_problem",
     "rms_chain",
     "rope_problem",
     "swiglu_problem",
@@ -54,6 +57,34 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return out
 
 
+def f32_to_e4m3_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to FP8 E4M3 (1 sign bit, 4 exponent bits with bias
+    7, 3 mantissa bits, no infinities; 0x7F/0xFF are NaN) with round-to-nearest-
+    even, saturating finite magnitudes above 448 (the largest finite value) to
+    448. Returns uint8 bit patterns.
+
+    The rounding is done in float64, where every step is exact: a magnitude
+    below 2^-6 is a multiple of 2^-9 (subnormal), otherwise 2^e (1 + m/8)."""
+    x = np.asarray(a, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    ax = np.minimum(np.abs(x), 448.0)
+    mant, exp = np.frexp(ax)            # ax = mant * 2^exp, mant in [0.5, 1)
+    e = exp - 1                         # ax = 2^e * (2 mant)
+    normal = ax >= 2.0 ** -6
+    # normal: (e + 7) * 8 + rint(8 * (2 mant - 1)); a carry out of the mantissa
+    # (rint gives 8) lands in the exponent field, as it should
+    code_n = (e + 7) * 8 + np.rint(16.0 * mant - 8.0)
+    # subnormal: multiples of 2^-9; rint gives 0..8, and 8 is the smallest normal (0x08)
+    code_s = np.rint(ax * 512.0)
+    code = np.where(normal, code_n, code_s)
+    code = np.minimum(code, 0x7E).astype(np.uint8)
+    out = code | sign
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = np.uint8(0x7F)
+    return out
+
+
 def _children(seed: int, n: int):
     return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(n)]
 
@@ -66,6 +97,28 @@ def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0, mean: float =
     if mean != 0.0:
         x += np.float32(mean)
     return f32_to_bf16_bits(x)
+
+
+def normal_e4m3(rng: np.random.Generator, shape) -> np.ndarray:
+    """E4M3 bits of N(0, 1) drawn in float32 (the tensor's value is a per-tensor
+    scale times these)."""
+    return f32_to_e4m3_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+def fp8_problem(M: int, K: int, N: int, seed: int = 0, labels: bool = False) -> dict:
+    """FP8 (E4M3) GEMM operands with per-tensor scales, for the FP8 mainloop:
+    A[M,K] = sA * e4m3(N(0,1)) with sA = 1 (activations), and the weight stored
+    K-major as B[N,K] = sB * e4m3(N(0,1)) with sB = 1/sqrt(K), so that the
+    weight is distributed as N(0, 1/K) like the bf16 workloads' and the product
+    is O(1). Returns the bit arrays and the float scales; with labels=True also
+    int32 labels uniform in [0, N) (the cross-entropy workload).
+    Tensors in spawn order: A, B, labels."""
+    g = _children(seed, 3)
+    out = {"A": normal_e4m3(g[0], (M, K)), "B": normal_e4m3(g[1], (N, K)),
+           "sA": 1.0, "sB": float(1.0 / np.sqrt(K))}
+    if labels:
+        out["labels"] = g[2].integers(0, N, size=(M,), dtype=np.int32)
+    return out
 
 
 def rms_chain(M: int, K: int, d: int, N2: int, seed: int = 0, bwd_K: int | None = None) -> dict:
@@ -192,5 +245,11 @@ WORKLOADS = {
                                bwd_K=8192),
     "lm_head_ce_8192": dict(kind="ce", M=8192, K=4096, V=32768),
 }
+# FP8 (E4M3) mainloop variants of the single-GEMM forward operators, same shapes
+# as their bf16 workloads; weights stored K-major ([N, K]).
+WORKLOADS["fp8_rope_qkv_4096"] = dict(kind="fp8_rope", M=4096, K=4096, N=12288, head_dim=128, theta=10000.0,
+                                      S=4096, rope_cols=8192)
+WORKLOADS["fp8_swiglu_up_4096"] = dict(kind="fp8_swiglu", M=4096, K=4096, N=28672)
+WORKLOADS["fp8_lm_head_ce_8192"] = dict(kind="fp8_ce", M=8192, K=4096, N=32768)
 for _d, _b in BLOCK_SIZES.items():
     WORKLOADS[f"block_d{_d}"] = dict(kind="block", S=4096, theta=10000.0, eps=1e-6, rope_cols=2 * _d, **_b)

@@ -10,6 +10,7 @@ import numpy as np
 
 __all__ = [
     "bf16",
+    "e4m3",
     "matmul",
     # GEMM-RMSNorm-GEMM forward
     "rms_scale",
@@ -67,6 +68,21 @@ def bf16(bits) -> np.ndarray:
     high half of an IEEE binary32."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def e4m3(bits) -> np.ndarray:
+    """Decode FP8 E4M3 bit patterns to float64: sign bit 7, exponent bits 6..3
+    with bias 7, mantissa bits 2..0. Exponent field 0 is subnormal,
+    (-1)^s 2^-6 (m/8); otherwise (-1)^s 2^(e-7) (1 + m/8). There are no
+    infinities; exponent 15 with mantissa 7 is NaN, so the largest finite
+    magnitude is 2^8 * 1.75 = 448."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sgn = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (b & 0x7 == 7), np.nan, mag)
+    return sgn * mag
 
 
 def matmul(A, B) -> np.ndarray:

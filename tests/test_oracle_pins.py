@@ -462,6 +462,8 @@ def test_golden_hand_values(case):
         got = O.ce_fwd(inp["logits"], inp["labels"])
     elif op == "ce_bwd":
         got = dict(dl=O.ce_bwd(inp["logits"], inp["labels"], inp["lse"], inp["grad_scale"]))
+    elif op == "e4m3":
+        got = dict(value=O.e4m3(np.asarray(inp["bits"], np.uint8)))
     else:
         raise AssertionError(op)
     for k, v in exp.items():
@@ -650,3 +652,47 @@ def test_block_inputs_generator():
     assert {k: v.shape for k, v in a.items()} == shapes
     w = O.bf16(gen.block_problem(64, 256, 512, with_bwd=False)["Wgu"])
     assert abs(w.std() * 16 - 1) < 0.02
+
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3: the oracle's decoder and the input generator's encoder
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decoder_matches_torch_float8():
+    """All 256 bit patterns against torch's float8_e4m3fn (a library decoder)."""
+    b = np.arange(256, dtype=np.uint8)
+    mine = O.e4m3(b)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.isnan(mine).sum() == 2  # 0x7F and 0xFF
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+    # monotone over the positive finite codes, largest 448
+    pos = mine[:0x7F]
+    assert np.all(np.diff(pos) > 0) and pos[-1] == 448.0
+
+
+def test_e4m3_encoder_rne_and_saturation():
+    R = rng(91)
+    x = (R.standard_normal(200000) * np.exp(R.uniform(-8, 6, 200000))).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ties = np.float32([1.0625, 1.1875, 3 * 2.0 ** -10, 5 * 2.0 ** -10, -9.0, 2.0 ** -6 - 2.0 ** -10, 0.0])
+    x = np.concatenate([x, ties])
+    enc = gen.f32_to_e4m3_bits(x)
+    assert np.array_equal(enc, torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    # round trip of every finite code is exact
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    assert np.array_equal(gen.f32_to_e4m3_bits(O.e4m3(codes).astype(np.float32)) & 0x7F, codes & 0x7F)
+    # saturation instead of NaN above 448
+    assert list(gen.f32_to_e4m3_bits(np.float32([500.0, -1e6, 464.0]))) == [0x7E, 0xFE, 0x7E]
+
+
+def test_fp8_problem_scales_and_determinism():
+    a = gen.fp8_problem(64, 256, 48, seed=2, labels=True)
+    b = gen.fp8_problem(64, 256, 48, seed=2)
+    assert np.array_equal(a["A"], b["A"]) and np.array_equal(a["B"], b["B"])
+    assert a["B"].shape == (48, 256) and a["sB"] == 1.0 / 16.0
+    w = O.e4m3(gen.fp8_problem(8, 4096, 512)["B"]) / 64.0
+    assert abs(w.std() * 64 - 1) < 0.02
