@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite")
     ap.add_argument("--only", default=None,
                     help="with --suite: run one workload (rmsnorm_chain_tiny, rmsnorm_chain_8192, rope_qkv_4096, "
-                         "swiglu_up_4096, lm_head_ce_8192, block_d2048, block_d4096, block_d8192)")
+                         "swiglu_up_4096, lm_head_ce_8192, block_d2048, block_d4096, block_d8192, fp8_rope_qkv_4096, "
+                         "fp8_swiglu_up_4096, fp8_lm_head_ce_8192)")
     return ap.parse_args()
 
 
@@ -472,7 +473,7 @@ def suite(a):
         e.synchronize()
         return s.elapsed_time(e)
 
-    def report(workload, op, flops, fused, unfused, launches):
+    def report(workload, op, flops, fused, unfused, launches, peak_mult=1.0):
         # fused and unfused repetitions alternate, so clock and power drift over
         # the run affect both columns alike
         for _ in range(3):
@@ -484,11 +485,14 @@ def suite(a):
             tu.append(once(unfused))
         fm, fmin = float(np.median(tf)), float(np.min(tf))
         um, umin = float(np.median(tu)), float(np.min(tu))
+        pk = peak_tf * peak_mult
         line = {"suite": workload, "op": op, "fused_ms": fm, "fused_min_ms": fmin, "unfused_ms": um,
                 "unfused_min_ms": umin, "speedup_vs_unfused": um / fm,
                 "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None,
-                "pct_bf16_peak": 100 * flops / (fm * 1e-3) / 1e12 / peak_tf if flops else None,
-                "kernels": launches, "peak": f"{peak_tf} TFLOP/s ({peak_kind})", "reps": a.reps}
+                "pct_bf16_peak": 100 * flops / (fm * 1e-3) / 1e12 / pk if flops else None,
+                "kernels": launches, "reps": a.reps,
+                "peak": (f"{pk:.1f} TFLOP/s ({peak_kind} bf16 x {peak_mult:g})" if peak_mult != 1.0
+                         else f"{peak_tf} TFLOP/s ({peak_kind})")}
         print(json.dumps(line), flush=True)
 
     # -- GEMM-RMSNorm-GEMM (tiny and 8192)
@@ -551,6 +555,7 @@ def suite(a):
     for dm in sorted(gen.BLOCK_SIZES):
         if want(f"block_d{dm}"):
             block_suite(G, gen, dev, report, dm)
+    fp8_suite(G, gen, dev, report, want)
     status = G.coda_device_status(clear=True)
     print(json.dumps({"suite": "done", "device_status": status}), flush=True)
     return 0 if status == 0 else 1
@@ -616,6 +621,73 @@ def ce_suite(G, gen, d, dev, report):
            lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
            lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
            "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel")
+
+
+def fp8_suite(G, gen, dev, report, want):
+    """FP8 (E4M3) mainloop variants: the fused kernel against the FP8 plain GEMM
+    plus the same stand-alone kernels. The percentage is of the FP8 dense peak,
+    taken as twice the measured BF16 peak (the nominal FP8 / BF16 ratio)."""
+    import torch
+
+    def u8(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).to(dev)
+
+    name = "fp8_rope_qkv_4096"
+    if want(name):
+        w = gen.WORKLOADS[name]
+        p = gen.fp8_problem(w["M"], w["K"], w["N"], seed=0)
+        X, Wt, al = u8(p["A"]), u8(p["B"]), p["sA"] * p["sB"]
+        c, sn = G.coda_rope_tables(w["S"], w["head_dim"], w["theta"], device=dev)
+        out = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        hd, rc = w["head_dim"], w["rope_cols"]
+        fl = 2.0 * w["M"] * w["N"] * w["K"]
+        report(name, "fwd", fl, lambda: G.coda_gemm_rope_fp8(X, Wt, al, c, sn, hd, rc, out=out),
+               lambda: (G.coda_gemm_fp8(X, Wt, al, out=out), G.coda_unfused_rope(out, c, sn, hd, rc)), "1 vs 2",
+               peak_mult=2.0)
+        report(name, "plain_gemm", fl, lambda: G.coda_gemm_fp8(X, Wt, al, out=out),
+               lambda: G.coda_gemm_fp8(X, Wt, al, out=out), "identity epilogue, both columns the same kernel",
+               peak_mult=2.0)
+        del p, X, Wt, out
+    name = "fp8_swiglu_up_4096"
+    if want(name):
+        w = gen.WORKLOADS[name]
+        p = gen.fp8_problem(w["M"], w["K"], w["N"], seed=0)
+        X, Wt, al = u8(p["A"]), u8(p["B"]), p["sA"] * p["sB"]
+        F = w["N"] // 2
+        A = torch.empty((w["M"], F), dtype=torch.bfloat16, device=dev)
+        GU = torch.empty((w["M"], 2 * F), dtype=torch.bfloat16, device=dev)
+        fl = 2.0 * w["M"] * w["N"] * w["K"]
+        report(name, "fwd", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A),
+               lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (no GU saved)",
+               peak_mult=2.0)
+        report(name, "fwd_save_gu", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A, gu=GU),
+               lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)),
+               "1 vs 2 (GU saved for backward)", peak_mult=2.0)
+        del p, X, Wt, A, GU
+    name = "fp8_lm_head_ce_8192"
+    if want(name):
+        w = gen.WORKLOADS[name]
+        p = gen.fp8_problem(w["M"], w["K"], w["N"], seed=0, labels=True)
+        H, Wt, al = u8(p["A"]), u8(p["B"]), p["sA"] * p["sB"]
+        y = torch.from_numpy(p["labels"]).to(dev)
+        logits = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        fl = 2.0 * w["M"] * w["N"] * w["K"]
+        st = {}
+
+        def fused_ce():
+            pm, ps, pa, tg = G.coda_gemm_ce_lse_fp8(H, Wt, al, y)
+            st["lse"] = G.coda_ce_reduce(pm, ps, pa, tg)[0]
+
+        report(name, "fwd", fl, fused_ce, lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits),
+                                                   G.coda_unfused_ce_fwd(logits, y)),
+               "GEMM+partials + reduce vs GEMM (bf16 logits) + CE", peak_mult=2.0)
+        fused_ce()
+        lse = st["lse"]
+        report(name, "bwd_dlogits", fl, lambda: G.coda_gemm_ce_bwd_fp8(H, Wt, al, y, lse, 1.0 / w["M"], out=logits),
+               lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / w["M"])),
+               "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel", peak_mult=2.0)
+        del p, H, Wt, logits
+    torch.cuda.empty_cache()
 
 
 def block_suite(G, gen, dev, report, dm):

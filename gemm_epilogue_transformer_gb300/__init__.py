@@ -25,7 +25,8 @@ __all__ = [
     "coda_unfused_rope", "coda_unfused_rope_bwd", "coda_unfused_ce_fwd", "coda_unfused_ce_bwd",
     "coda_unfused_rowdot", "coda_unfused_rmsnorm_bwd", "coda_gemm_rowscale_rope", "coda_gemm_rowscale_swiglu",
     "coda_gemm_swiglu_bwd_rowdot", "coda_gemm_rmsnorm_bwd_res", "coda_rope_bwd_rowdot",
-    "coda_block_workspace_bytes", "CodaBlock",
+    "coda_block_workspace_bytes", "CodaBlock", "coda_gemm_fp8", "coda_gemm_rope_fp8", "coda_gemm_swiglu_fp8",
+    "coda_gemm_ce_lse_fp8", "coda_gemm_ce_bwd_fp8",
 ]
 
 
@@ -541,3 +542,85 @@ class CodaBlock:
 
     def bwd_unfused(self, stream=None):
         return self._run("coda_block_bwd_unfused", stream)
+
+
+# ----------------------------------------------------------------- FP8 (E4M3) mainloop
+
+def _e4m3(t, name):
+    """E4M3 operands travel as uint8 tensors (or torch.float8_e4m3fn, viewed as bytes)."""
+    if t.dtype != torch.uint8:
+        if str(t.dtype) != "torch.float8_e4m3fn":
+            raise TypeError(f"{name} must be a CUDA uint8 or float8_e4m3fn tensor (got {t.dtype})")
+        t = t.view(torch.uint8)
+    if not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+        raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    return t
+
+
+def coda_gemm_fp8(A, B, alpha: float, out=None, stream=None):
+    """C = alpha A B^T with A [M,K], B [N,K] E4M3; C bf16 [M,N]."""
+    A, B = _e4m3(A, "A"), _e4m3(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("shape mismatch")
+    out = _empty((M, N), torch.bfloat16, A) if out is None else out
+    _check(lib().coda_gemm_fp8(M, N, K, _ptr(A), _ptr(B), float(alpha), _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_rope_fp8(X, W, alpha: float, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
+    X, W = _e4m3(X, "X"), _e4m3(W, "W")
+    _f32(cos, "cos"), _f32(sin, "sin")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or cos.shape[1] != head_dim // 2:
+        raise ValueError("shape mismatch")
+    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    _check(lib().coda_gemm_rope_fp8(M, N, K, _ptr(X), _ptr(W), float(alpha), _ptr(cos), _ptr(sin), cos.shape[0],
+                                    head_dim, rope_cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def coda_gemm_swiglu_fp8(X, Wgu, alpha: float, want_gu: bool = False, out=None, gu=None, stream=None):
+    """A = silu(G) * U on GU = alpha X Wgu^T, Wgu [2F, K] (rows gate/up interleaved); returns (A, GU or None)."""
+    X, Wgu = _e4m3(X, "X"), _e4m3(Wgu, "Wgu")
+    M, K = X.shape
+    F2 = Wgu.shape[0]
+    if Wgu.shape[1] != K or F2 % 2:
+        raise ValueError("shape mismatch")
+    F = F2 // 2
+    out = _empty((M, F), torch.bfloat16, X) if out is None else out
+    if want_gu and gu is None:
+        gu = _empty((M, F2), torch.bfloat16, X)
+    _check(lib().coda_gemm_swiglu_fp8(M, F, K, _ptr(X), _ptr(Wgu), float(alpha), _ptr(out), _ptr(gu),
+                                      _stream(stream)))
+    return out, gu
+
+
+def coda_gemm_ce_lse_fp8(H, W, alpha: float, labels, with_argmax: bool = True, stream=None):
+    H, W = _e4m3(H, "H"), _e4m3(W, "W")
+    _i32(labels, "labels")
+    M, K = H.shape
+    V = W.shape[0]
+    if W.shape[1] != K or labels.shape[0] != M:
+        raise ValueError("shape mismatch")
+    nb = coda_num_col_tiles(V)
+    pmax = _empty((M, nb), torch.float32, H)
+    psum = _empty((M, nb), torch.float32, H)
+    parg = _empty((M, nb), torch.int32, H) if with_argmax else None
+    tgt = _empty((M,), torch.float32, H)
+    _check(lib().coda_gemm_ce_lse_fp8(M, V, K, _ptr(H), _ptr(W), float(alpha), _ptr(labels), _ptr(pmax), _ptr(psum),
+                                      _ptr(parg), _ptr(tgt), _stream(stream)))
+    return pmax, psum, parg, tgt
+
+
+def coda_gemm_ce_bwd_fp8(H, W, alpha: float, labels, lse, grad_scale: float, out=None, stream=None):
+    H, W = _e4m3(H, "H"), _e4m3(W, "W")
+    _i32(labels, "labels"), _f32(lse, "lse")
+    M, K = H.shape
+    V = W.shape[0]
+    out = _empty((M, V), torch.bfloat16, H) if out is None else out
+    _check(lib().coda_gemm_ce_bwd_fp8(M, V, K, _ptr(H), _ptr(W), float(alpha), _ptr(labels), _ptr(lse),
+                                      float(grad_scale), _ptr(out), _stream(stream)))
+    return out

@@ -75,6 +75,11 @@ SIGNATURES = {
     "coda_gemm_swiglu_bwd_rowdot": (I, [I, I, I, P, P, P, P, P, P, P]),
     "coda_gemm_rmsnorm_bwd_res": (I, [I, I, I, P, P, P, P, P, P, P, P, P, P]),
     "coda_rope_bwd_rowdot": (I, [I, I, P, P, P, P, P, I, I, I, I, P, P, P]),
+    "coda_gemm_fp8": (I, [I, I, I, P, P, c_float, P, P]),
+    "coda_gemm_rope_fp8": (I, [I, I, I, P, P, c_float, P, P, I, I, I, P, P]),
+    "coda_gemm_swiglu_fp8": (I, [I, I, I, P, P, c_float, P, P, P]),
+    "coda_gemm_ce_lse_fp8": (I, [I, I, I, P, P, c_float, P, P, P, P, P, P]),
+    "coda_gemm_ce_bwd_fp8": (I, [I, I, I, P, P, c_float, P, P, c_float, P, P]),
     "coda_block_workspace_bytes": (c_size_t, [I, I, I, I]),
     "coda_block_fwd": (I, [BLK, P]),
     "coda_block_fwd_noalloc": (I, [BLK, P]),

@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcoda.so")
 
-SOURCES = ["runtime.cu", "aux.cu", "unfused.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_chain.cu", "block.cu"]
+SOURCES = ["runtime.cu", "aux.cu", "unfused.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_chain.cu", "block.cu",
+           "gemm_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -89,6 +89,7 @@ struct GemmShape {
   int* status;                    // device status word (CODA_DEVST_* bits)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
   int inject;                     // test hook: 1 = producers skip their first stage fill
+  float alpha;                    // FP8 mainloop: product of the operands' per-tensor scales
 };
 
 struct EpiCtx {
@@ -247,7 +248,11 @@ __device__ __forceinline__ void unpack32(const uint4 (&u)[4], float (&v)[32]) {
 //   __device__ static void store_coord(const Params&, const EpiCtx&, int c, int slot, int& map, int& x, int& y);
 //   __device__ static void end(State&, const Params&, const EpiCtx&);
 // ---------------------------------------------------------------------------
-template <class Epi, int kCG>
+// kF8: the FP8 mainloop. A and B are E4M3, K-major; a stage holds 128 K
+// elements (the same 128-byte rows, so the same shared-memory layout, boxes and
+// descriptors as bf16), the MMAs are kind::f8f6f4 with K = 32, and the
+// accumulator is scaled by p.alpha before the epilogue program sees it.
+template <class Epi, int kCG, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb_target = kCG == 2 ? mapa_shared(fb, 0) : fb;
           const uint32_t a_dst = s_base + stage * C::kStageBytes;
           const uint32_t b_dst = a_dst + C::kABytes;
-          const int k0 = kb * BK;
+          const int k0 = kb * (kF8 ? 2 * BK : BK);  // elements: one 128-byte row per stage either way
           auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
             if constexpr (kCG == 2)
               tma_load_2d_pair(dst, m, fb_target, x, y);
@@ -401,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (lane == 0 && leader) {
       const int amn = p.a_mn != 0, bmn = p.b_mn != 0;
-      const uint32_t idesc_full = idesc_bf16_f32(C::kTileM, BN, amn, bmn);
-      const uint32_t idesc_half = idesc_bf16_f32(C::kTileM, BSEG, amn, bmn);
+      const uint32_t idesc_full = kF8 ? idesc_e4m3_f32(C::kTileM, BN) : idesc_bf16_f32(C::kTileM, BN, amn, bmn);
+      const uint32_t idesc_half = kF8 ? idesc_e4m3_f32(C::kTileM, BSEG) : idesc_bf16_f32(C::kTileM, BSEG, amn, bmn);
       // Operand descriptors. K-major: 128B rows, 8-row groups 1024B apart,
       // K advances 32B (16 bf16) inside the swizzle atom. MN-major: 64-element
       // MN chunks 8192B apart (LBO), 8-row K groups 1024B apart (SBO), K
@@ -432,10 +437,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024u);
-            if constexpr (kCG == 2)
-              tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            else
-              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            const uint32_t acc_in = (kb > 0 || k > 0) ? 1u : 0u;
+            if constexpr (kF8) {
+              if constexpr (kCG == 2)
+                tc_mma_f8_pair(d_tmem, ad, bd, idesc, acc_in);
+              else
+                tc_mma_f8(d_tmem, ad, bd, idesc, acc_in);
+            } else {
+              if constexpr (kCG == 2)
+                tc_mma_bf16_pair(d_tmem, ad, bd, idesc, acc_in);
+              else
+                tc_mma_bf16(d_tmem, ad, bd, idesc, acc_in);
+            }
           }
           if constexpr (kCG == 2)
             tc_commit_pair(empty_bar(stage), 0x3);
@@ -559,6 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.k_blocks == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+          }
+          if constexpr (kF8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] *= p.alpha;
           }
           // this store step's boxes are contiguous: box k at box0 + k * kStageBoxBytes
           const uint32_t box0 = my_stage + (sbuf * kSlots) * kStageBoxBytes;

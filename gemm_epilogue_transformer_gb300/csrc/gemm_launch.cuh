@@ -35,11 +35,13 @@ inline int rope_table_maps(int tma, const float* c, const float* s, int S, int h
   return make_map_f32(ts, s, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <class Epi, int kCG>
+// kF8: E4M3 operands, K-major only (A [M, K], B stored [N, K], lda / ldb in
+// bytes = elements), 128-element K stages, accumulator scaled by alpha.
+template <class Epi, int kCG, bool kF8 = false>
 int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, const void* A, int lda, int a_mn,
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
                    const CUtensorMap& i0, const CUtensorMap& i1, const typename Epi::Params& ep,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, float alpha = 1.0f) {
   using C = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
@@ -49,7 +51,13 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   // 3-D box per stage (mode 2) instead of one 2-D box per 64 columns (mode 1).
   if (a_mn && M % 64 == 0) a_mn = 2;
   if (b_mn && N % 64 == 0) b_mn = 2;
-  if (K > 0) {
+  if (kF8 && K > 0) {
+    if (a_mn || b_mn) return fail(CODA_ERR_UNSUPPORTED, "%s: FP8 operands must be K-major", fn);
+    rc = make_map_u8(&tA, A, K, M, static_cast<uint64_t>(lda), 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    rc = make_map_u8(&tB, B, K, N, static_cast<uint64_t>(ldb), 2 * BK, C::kBLoad, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  } else if (K > 0) {
     if (a_mn == 2)
       rc = make_map_bf16_mn3d(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, BM / 64);
     else if (a_mn)
@@ -65,7 +73,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
       rc = make_map_bf16(&tB, B, K, N, static_cast<uint64_t>(ldb) * 2u, 64, C::kBLoad, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
-  auto kernel = &gemm_epilogue_kernel<Epi, kCG>;
+  auto kernel = &gemm_epilogue_kernel<Epi, kCG, kF8>;
   static int max_clusters[64] = {0};  // per device; 0 = not yet queried
   int dev = 0;
   cudaGetDevice(&dev);
@@ -105,7 +113,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.b_mn = b_mn;
   p.m_blocks = (M + C::kTileM - 1) / C::kTileM;
   p.n_blocks = (N + BN - 1) / BN;
-  p.k_blocks = (K + BK - 1) / BK;
+  p.k_blocks = kF8 ? (K + 2 * BK - 1) / (2 * BK) : (K + BK - 1) / BK;
   p.num_tiles = p.m_blocks * p.n_blocks;
   p.group_m = p.m_blocks < kGroupM / kCG ? p.m_blocks : kGroupM / kCG;
   p.seg_blocks = (N + BSEG - 1) / BSEG;
@@ -122,6 +130,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.status = di->status;
   p.timeout_ns = wait_timeout_ns();
   p.inject = take_injected_fault();
+  p.alpha = alpha;
 
   const int clusters = p.num_items < cmax ? p.num_items : cmax;
   cfg.gridDim = dim3(clusters * kCG, 1, 1);
@@ -137,16 +146,18 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
 // coda_set_cta_group() fixed the choice.
 // o0 / o1: TMA store targets; i0 / i1: TMA sources of the epilogue's input
 // boxes (unused maps may be any valid map).
-template <class Epi>
+template <class Epi, bool kF8 = false>
 int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, int a_mn, const void* B, int ldb,
                  int b_mn, const CUtensorMap& o0, const CUtensorMap& o1, const CUtensorMap& i0,
-                 const CUtensorMap& i1, const typename Epi::Params& ep, cudaStream_t stream) {
+                 const CUtensorMap& i1, const typename Epi::Params& ep, cudaStream_t stream, float alpha = 1.0f) {
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int forced = cta_group_setting();
   const int g = forced ? forced : (M > BM ? 2 : 1);
-  if (g == 2) return launch_variant<Epi, 2>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream);
-  return launch_variant<Epi, 1>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream);
+  if (g == 2)
+    return launch_variant<Epi, 2, kF8>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream,
+                                       alpha);
+  return launch_variant<Epi, 1, kF8>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream, alpha);
 }
 
 }  // namespace coda

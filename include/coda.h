@@ -273,6 +273,42 @@ int coda_unfused_rowdot(int M, int N, int d, const coda_bf16* dY, const coda_bf1
 int coda_unfused_rmsnorm_bwd(int M, int d, const coda_bf16* G, const coda_bf16* h, const coda_bf16* gamma,
                              const float* r, coda_bf16* dh_out, float* pdg_out, coda_stream_t stream);
 
+/* ------------------------------------------------- FP8 (E4M3) mainloop (f3)
+ * CODA note, research background: as FP8 and FP4 GEMMs multiply the tensor
+ * throughput, the memory-bound operators around the GEMM take a larger share
+ * of the time, which the fused epilogues remove. These entry points run the
+ * same epilogue programs as their bf16 twins on an FP8 mainloop (tcgen05
+ * kind::f8f6f4, fp32 accumulators in TMEM):
+ *   - A [M,K] and B stored [N,K] (both K-major; B in the layout of a linear
+ *     layer's weight [out, in]) are E4M3 bytes: 1 sign bit, 4 exponent bits
+ *     with bias 7, 3 mantissa bits, no infinities (0x7F / 0xFF are NaN);
+ *   - the accumulator is multiplied by alpha, the product of the two operands'
+ *     per-tensor scales, before the epilogue program sees it;
+ *   - K a multiple of 16 (16-byte rows), N a multiple of 8; base pointers
+ *     16-byte aligned. Outputs, statistics, status bits and errors as the bf16
+ *     twins. */
+
+/* C[M,N] = alpha A B^T in bf16 (identity epilogue). */
+int coda_gemm_fp8(int M, int N, int K, const uint8_t* A, const uint8_t* B, float alpha, coda_bf16* C,
+                  coda_stream_t stream);
+
+/* coda_gemm_rope on P = alpha X W^T: X [M,K], W [N,K] E4M3. */
+int coda_gemm_rope_fp8(int M, int N, int K, const uint8_t* X, const uint8_t* W, float alpha, const float* cos_tab,
+                       const float* sin_tab, int S, int head_dim, int rope_cols, coda_bf16* out, coda_stream_t stream);
+
+/* coda_gemm_swiglu on GU = alpha X Wgu^T: Wgu [2F,K] E4M3, row 2f the gate and
+ * row 2f+1 the up projection of output f. gu_out (bf16 [M,2F]) may be NULL. */
+int coda_gemm_swiglu_fp8(int M, int F, int K, const uint8_t* X, const uint8_t* Wgu, float alpha, coda_bf16* A_out,
+                         coda_bf16* gu_out, coda_stream_t stream);
+
+/* coda_gemm_ce_lse on the logits alpha H W^T: H [M,K], W [V,K] E4M3. */
+int coda_gemm_ce_lse_fp8(int M, int V, int K, const uint8_t* H, const uint8_t* W, float alpha, const int32_t* labels,
+                         float* pmax_out, float* psum_out, int32_t* parg_out, float* tgt_out, coda_stream_t stream);
+
+/* coda_gemm_ce_bwd on the recomputed logits alpha H W^T. */
+int coda_gemm_ce_bwd_fp8(int M, int V, int K, const uint8_t* H, const uint8_t* W, float alpha, const int32_t* labels,
+                         const float* lse, float grad_scale, coda_bf16* dl_out, coda_stream_t stream);
+
 /* ------------------------------------------------------ block-level chain (f1)
  * CODA note, block-level ablation: a Transformer block seen as two
  * consecutive GEMM-Residual-RMSNorm-GEMM structures, one on the RoPE path and

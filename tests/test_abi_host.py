@@ -154,3 +154,14 @@ def test_block_chain_host_validation(lib):
     assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 16, 40, 32, good, good,
                                     None) == INVALID
     assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 16, 48, 0, good, good, None) == INVALID
+
+
+def test_fp8_host_validation(lib):
+    INVALID, UNSUPPORTED = -1, -2
+    good = _p(0x10000)
+    assert lib.coda_gemm_fp8(8, 16, 24, good, good, 1.0, good, None) == UNSUPPORTED      # K % 16
+    assert lib.coda_gemm_fp8(8, 12, 32, good, good, 1.0, good, None) == UNSUPPORTED      # N % 8
+    assert lib.coda_gemm_fp8(8, 16, 32, good, good, float("inf"), good, None) == INVALID
+    assert lib.coda_gemm_fp8(8, 16, 32, _p(0x10008), good, 1.0, good, None) == INVALID  # misaligned A
+    assert lib.coda_gemm_rope_fp8(8, 256, 32, good, good, 1.0, good, good, 16, 48, 128, good, None) == UNSUPPORTED
+    assert lib.coda_gemm_swiglu_fp8(8, 12, 32, good, good, 1.0, good, None, None) == UNSUPPORTED
