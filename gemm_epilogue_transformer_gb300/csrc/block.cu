@@ -21,8 +21,6 @@ using namespace coda;
 
 namespace {
 
-inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
-
 __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll

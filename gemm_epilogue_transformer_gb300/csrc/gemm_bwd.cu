@@ -5,22 +5,6 @@
 
 using namespace coda;
 
-namespace {
-
-inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
-
-int check_fused(const char* fn, int M, int N, int K, const void* A, const void* B) {
-  CODA_REQUIRE(M >= 0 && N >= 0 && K >= 0, CODA_ERR_INVALID, "%s: negative dimension (M=%d N=%d K=%d)", fn, M, N, K);
-  CODA_REQUIRE(N % 8 == 0 && K % 8 == 0, CODA_ERR_UNSUPPORTED, "%s: N=%d and K=%d must be multiples of 8", fn, N, K);
-  if (M > 0 && N > 0 && K > 0) {
-    CODA_REQ_PTR16(A);
-    CODA_REQ_PTR16(B);
-  }
-  return CODA_OK;
-}
-
-}  // namespace
-
 extern "C" {
 
 int coda_gemm_swiglu_bwd(int M, int F, int K, const coda_bf16* dY, const coda_bf16* Wd, const coda_bf16* gu,

@@ -10,8 +10,6 @@ using namespace coda;
 
 namespace {
 
-inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
-
 // Checks shared by the FP8 entry points: dims, 16-byte rows of the K-major
 // E4M3 operands (K % 16) and of the bf16 outputs (N % 8), a finite alpha.
 int check_fp8(const char* fn, int M, int N, int K, const void* A, const void* B, float alpha) {

@@ -19,6 +19,18 @@ inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, in
                        static_cast<uint64_t>(ld) * 2u, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Checks shared by the fused bf16 entry points: non-negative dims, 8-element
+// granularity of N and K (16-byte rows), aligned operand pointers.
+inline int check_fused(const char* fn, int M, int N, int K, const void* A, const void* B) {
+  CODA_REQUIRE(M >= 0 && N >= 0 && K >= 0, CODA_ERR_INVALID, "%s: negative dimension (M=%d N=%d K=%d)", fn, M, N, K);
+  CODA_REQUIRE(N % 8 == 0 && K % 8 == 0, CODA_ERR_UNSUPPORTED, "%s: N=%d and K=%d must be multiples of 8", fn, N, K);
+  if (M > 0 && N > 0 && K > 0) {
+    CODA_REQ_PTR16(A);
+    CODA_REQ_PTR16(B);
+  }
+  return CODA_OK;
+}
+
 // TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16
 // frequencies (64 bytes) per box. Used when S % 32 == 0, so that a warp's 32
 // rows never wrap inside a box; otherwise the epilogue loads the tables directly.

@@ -28,6 +28,9 @@ int cta_group_setting();
 // Consume the one-shot test fault set by coda_test_inject_missing_load().
 int take_injected_fault();
 
+// The C ABI's opaque stream handle as a CUDA stream.
+inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
 // ---------------------------------------------------------------- checks
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

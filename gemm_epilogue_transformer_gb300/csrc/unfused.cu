@@ -10,7 +10,6 @@ using namespace coda;
 
 namespace {
 
-inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float exp_f(float x) { return exp2f(x * kLog2e); }
 
