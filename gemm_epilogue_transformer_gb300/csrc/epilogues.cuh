@@ -321,8 +321,12 @@ struct EpiRope {
       }
     }
   }
+  // One store box per chunk, and a one-chunk table ring (the slices are L2
+  // resident): the shared memory saved buys a sixth mainloop stage, which
+  // measured 1.7 % faster than five stages with a two-chunk ring.
   static constexpr int kChunksPerStore = 1;
-  static constexpr int kMaxSlots = 2;
+  static constexpr int kMaxSlots = 1;
+  static constexpr int kInRingBytes = 4096;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;

@@ -28,6 +28,8 @@
 // returns. No trap, no unbounded spin.
 #pragma once
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "../../include/coda.h"
 
@@ -50,12 +52,12 @@ constexpr int kMaxInSlots = 4;
 // Per-variant constants. kCG = 1: one SM computes a 128 x 256 tile. kCG = 2:
 // an SM pair (cta_group::2) computes a 256 x 256 tile; each CTA holds its 128
 // rows of A and half (128 columns) of B, so a stage is 32 KiB per SM instead
-// of 48 KiB and the ring is 6 deep instead of 4. kIn = input boxes per chunk
-// (0, 1, 2): epilogues with inputs give one mainloop stage to the input ring
-// (a 5-deep ring measured as fast as a 6-deep one for the pair variant).
-// kSlots = store boxes per staging buffer (2, or 3 for SwiGLU with its
-// pre-activation side output, which also takes the shorter ring).
-template <int kCG, int kIn, int kSlots>
+// of 48 KiB. kIn = input boxes per chunk (0, 1, 2), kInWarp = bytes of each
+// epilogue warp's input ring, kSlots = store boxes per staging buffer (1-3).
+// The mainloop gets as many stages as the shared memory left after the
+// epilogue's staging and input ring allows, at most 6 (pair) or 4 (single):
+// 6 / 4 without inputs, 5 / 3 with an 8 KiB ring or three staging boxes.
+template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes>
 struct Cfg {
   static constexpr int kTileM = BM * kCG;
   static constexpr int kBLoad = BN / kCG;  // B columns loaded per CTA
@@ -63,16 +65,33 @@ struct Cfg {
   static constexpr int kBBytes = kBLoad * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiWarpBytes = kStageBoxBytes * kSlots * kEpiBufs;
-  static constexpr bool kShortRing = kIn > 0 || kSlots > 2;
-  static constexpr int kStages = kCG == 1 ? (kShortRing ? 3 : 4) : (kShortRing ? 5 : 6);
-  static constexpr int kInSlots = kIn ? kInWarpBytes / (kIn * kInBoxBytes) : 0;
-  static constexpr int kInBytes = kIn ? kEpiWarps * kInWarpBytes : 0;
+  static constexpr int kInSlots = kIn ? kInWarp / (kIn * kInBoxBytes) : 0;
+  static constexpr int kInBytes = kIn ? kEpiWarps * kInWarp : 0;
+  // As many mainloop stages as the rest of shared memory leaves room for, at
+  // most 6 (SM pair) or 4 (single SM).
+  static constexpr int kFixedBytes = 1024 + kEpiWarps * kEpiWarpBytes + kInBytes + 16 +
+                                     8 * (2 + 2 + 1 + kEpiWarps * kMaxInSlots);
+  static constexpr int kFitStages = (232448 - kFixedBytes) / (kStageBytes + 16);
+  static constexpr int kMaxStages = kCG == 2 ? 6 : 4;
+  static constexpr int kStages = kFitStages < kMaxStages ? kFitStages : kMaxStages;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kInSlots <= kMaxInSlots, "input ring slots");
-  static_assert(kSlots == 2 || kSlots == 3, "staging slots");
+  static_assert(kStages >= 3, "mainloop ring");
+  static_assert(kInSlots <= kMaxInSlots && (kIn == 0 || kInSlots >= 1), "input ring slots");
+  static_assert(kSlots >= 1 && kSlots <= 3, "staging slots");
+};
+
+// Per-epilogue input-ring size: kInWarpBytes unless the epilogue declares
+// kInRingBytes (a smaller ring can buy a mainloop stage).
+template <class E, class = void>
+struct InRingOf {
+  static constexpr int value = kInWarpBytes;
+};
+template <class E>
+struct InRingOf<E, std::void_t<decltype(E::kInRingBytes)>> {
+  static constexpr int value = E::kInRingBytes;
 };
 
 constexpr int BSEG = 128;  // epilogue segment: columns per partial-statistics block
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const GemmShape p, const typename Epi::Params ep) {
   constexpr int kIn = Epi::kInBoxes;
   constexpr int kSlots = Epi::kMaxSlots;
-  using C = Cfg<kCG, kIn, kSlots>;
+  using C = Cfg<kCG, kIn, kSlots, InRingOf<Epi>::value>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
@@ -506,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Input ring: lane 0 keeps up to kInSlots chunks' input boxes in flight,
     // running ahead across segments and work items; every lane consumes them
     // in the same order.
-    const uint32_t in_base = smem_u32(s_in) + ew * kInWarpBytes;
+    const uint32_t in_base = smem_u32(s_in) + ew * InRingOf<Epi>::value;
     uint32_t seq_used = 0;    // chunks consumed (all lanes)
     uint32_t seq_issued = 0;  // chunks issued (lane 0)
     int it_t = cluster_id, it_s = 0, it_c = 0;  // issue cursor (lane 0)
