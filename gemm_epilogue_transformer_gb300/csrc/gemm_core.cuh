@@ -57,14 +57,15 @@ constexpr int kMaxInSlots = 4;
 // The mainloop gets as many stages as the shared memory left after the
 // epilogue's staging and input ring allows, at most 6 (pair) or 4 (single):
 // 6 / 4 without inputs, 5 / 3 with an 8 KiB ring or three staging boxes.
-template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes>
+template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes, int kBufs = kEpiBufs>
 struct Cfg {
   static constexpr int kTileM = BM * kCG;
   static constexpr int kBLoad = BN / kCG;  // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = kBLoad * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiWarpBytes = kStageBoxBytes * kSlots * kEpiBufs;
+  static constexpr int kStageBufs = kBufs;  // staging buffers per warp (2, or 1 to buy a stage)
+  static constexpr int kEpiWarpBytes = kStageBoxBytes * kSlots * kBufs;
   static constexpr int kInSlots = kIn ? kInWarp / (kIn * kInBoxBytes) : 0;
   static constexpr int kInBytes = kIn ? kEpiWarps * kInWarp : 0;
   // As many mainloop stages as the rest of shared memory leaves room for, at
@@ -81,6 +82,17 @@ struct Cfg {
   static_assert(kStages >= 3, "mainloop ring");
   static_assert(kInSlots <= kMaxInSlots && (kIn == 0 || kInSlots >= 1), "input ring slots");
   static_assert(kSlots >= 1 && kSlots <= 3, "staging slots");
+  static_assert(kBufs == 1 || kBufs == 2, "staging buffers");
+};
+
+// Per-epilogue staging buffers: two unless the epilogue declares kStageBufs.
+template <class E, class = void>
+struct StageBufsOf {
+  static constexpr int value = kEpiBufs;
+};
+template <class E>
+struct StageBufsOf<E, std::void_t<decltype(E::kStageBufs)>> {
+  static constexpr int value = E::kStageBufs;
 };
 
 // Per-epilogue input-ring size: kInWarpBytes unless the epilogue declares
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const GemmShape p, const typename Epi::Params ep) {
   constexpr int kIn = Epi::kInBoxes;
   constexpr int kSlots = Epi::kMaxSlots;
-  using C = Cfg<kCG, kIn, kSlots, InRingOf<Epi>::value>;
+  using C = Cfg<kCG, kIn, kSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
@@ -601,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t box1 = box0 + kStageBoxBytes;
           if (nslots > 0 && (cs % Epi::kChunksPerStore) == 0) {
             // the staging buffer about to be written was last read by the store
-            // group before the most recent one
-            if (lane == 0) bulk_wait_read<1>();
+            // group kStageBufs groups back
+            if (lane == 0) bulk_wait_read<C::kStageBufs - 1>();
             __syncwarp();
           }
           Epi::chunk(st, ep, cx, cs, acc, pre, in, box0, box1);
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               bulk_commit();
             }
-            sbuf ^= 1;
+            if constexpr (C::kStageBufs == 2) sbuf ^= 1;
           }
         };
         // vector operands: chunk c+1's loads are issued before chunk c runs

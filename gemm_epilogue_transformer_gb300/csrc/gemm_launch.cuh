@@ -54,7 +54,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
                    const CUtensorMap& i0, const CUtensorMap& i1, const typename Epi::Params& ep,
                    cudaStream_t stream, float alpha = 1.0f) {
-  using C = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value>;
+  using C = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
