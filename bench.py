@@ -464,6 +464,22 @@ def suite(a):
     def d(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
+    def graph_of(fn):
+        """Capture fn's launches into a CUDA graph (after one direct run) and return its replay."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        graphs.append(g)
+        return g.replay
+
+    graphs = []
+
     def once(fn):
         flush.zero_()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -525,6 +541,10 @@ def suite(a):
             G.coda_gemm(nn, W1, out=Y)
 
         report(name, "fwd", 2 * 2.0 * M * Kd * d_, fused_fwd, unfused_fwd, "3 fused (2 GEMM + aux) vs 4 unfused")
+        if M * Kd <= 256 * 512:
+            # the tiny chain is launch-bound: the same sequences replayed from CUDA graphs
+            report(name, "fwd_graph", 2 * 2.0 * M * Kd * d_, graph_of(fused_fwd), graph_of(unfused_fwd),
+                   "the same launches, each sequence replayed from one CUDA graph")
         fused_fwd()
 
         def fused_bwd():

@@ -41,3 +41,58 @@ def test_missing_load_times_out_and_context_survives(coda, cg):
     C = coda.coda_gemm(dA, dB)
     assert coda.coda_device_status(clear=True) == 0
     assert_bf16(f64(C), O.matmul(O.bf16(A), O.bf16(B)), "GEMM after the aborted launch")
+
+
+def _rope_case(coda):
+    p = gen.rope_problem(512, 256, 768, seed=4)
+    c, s = coda.coda_rope_tables(4096, 128, 10000.0)
+    X, W = dev_bf16(p["X"]), dev_bf16(p["W"])
+    run = lambda: coda.coda_gemm_rope(X, W, c, s, 128, 512)  # noqa: E731
+    ref = O.gemm_rope(O.bf16(p["X"]), O.bf16(p["W"]), np.arange(512), 128, 10000.0, 512)
+    return run, ref
+
+
+def _swiglu_bwd_case(coda):
+    p = gen.swiglu_problem(512, 256, 384, seed=5)
+    GU = gen.normal_bf16(np.random.default_rng(5), (512, 768))
+    dY, Wd, gu = dev_bf16(p["dY"]), dev_bf16(p["Wd"]), dev_bf16(GU)
+    run = lambda: coda.coda_gemm_swiglu_bwd(dY, Wd, gu)  # noqa: E731
+    ref = O.gemm_swiglu_bwd(O.bf16(p["dY"]), O.bf16(p["Wd"]), O.bf16(GU))["dGU"]
+    return run, ref
+
+
+def _fp8_case(coda):
+    import torch
+    p = gen.fp8_problem(512, 256, 512, seed=6)
+    A = torch.from_numpy(p["A"]).cuda()
+    B = torch.from_numpy(p["B"]).cuda()
+    alpha = p["sA"] * p["sB"]
+    run = lambda: coda.coda_gemm_fp8(A, B, alpha)  # noqa: E731
+    ref = O.matmul(O.e4m3(p["A"]), O.e4m3(p["B"]).T) * alpha
+    return run, ref
+
+
+@pytest.mark.parametrize("case", [_rope_case, _swiglu_bwd_case, _fp8_case], ids=["rope_tma_tables", "swiglu_bwd_inputs",
+                                                                             "fp8_mainloop"])
+@pytest.mark.parametrize("cg", [1, 2], ids=["cta1", "cta2"])
+def test_abort_with_epilogue_inputs_in_flight(coda, cg, case):
+    """The same missing fill in kernels whose epilogue warps already have TMA
+    input boxes in flight (RoPE tables, SwiGLU pre-activations) and in the FP8
+    mainloop: the abort path drains them, and the context stays usable."""
+    run, ref = case(coda)
+    try:
+        coda.coda_set_cta_group(cg)
+        coda.coda_set_wait_timeout_ns(2_000_000)
+        assert coda.coda_device_status(clear=True) == 0
+        coda.coda_test_inject_missing_load()
+        t0 = time.perf_counter()
+        run()
+        st = coda.coda_device_status(clear=True)
+        assert st & CODA_DEVST_TIMEOUT, f"status {st}"
+        assert time.perf_counter() - t0 < 5.0
+    finally:
+        coda.coda_set_wait_timeout_ns(2_000_000_000)
+        coda.coda_set_cta_group(0)
+    out = run()
+    assert coda.coda_device_status(clear=True) == 0
+    assert_bf16(f64(out), ref, "result after the aborted launch")
