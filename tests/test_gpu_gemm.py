@@ -91,3 +91,25 @@ def test_gemm_leading_dimensions(coda, cta_group, ta, tb):
     a = O.bf16(A).T if ta else O.bf16(A)
     b = O.bf16(B).T if tb else O.bf16(B)
     assert_bf16(f64(C), O.matmul(a, b), f"strided gemm ta={ta} tb={tb}")
+
+
+def test_gemm_random_shapes(coda):
+    """Seeded sweep: random sizes (multiples of 8; some multiples of 64, which
+    take the 3-D operand boxes), random operand layouts, both tile variants."""
+    R = np.random.default_rng(2024)
+    for i in range(24):
+        M = int(R.integers(1, 96)) * 8
+        N = int(R.integers(1, 96)) * 8
+        K = int(R.integers(1, 64)) * 8
+        if i % 3 == 0:
+            M, N = 64 * max(1, M // 64), 64 * max(1, N // 64)
+        ta, tb, cg = int(R.integers(0, 2)), int(R.integers(0, 2)), int(R.integers(1, 3))
+        A, B = _operands(M, N, K, ta, tb, seed=1000 + i)
+        try:
+            coda.coda_set_cta_group(cg)
+            C = coda.coda_gemm(dev_bf16(A), dev_bf16(B), transA=bool(ta), transB=bool(tb))
+        finally:
+            coda.coda_set_cta_group(0)
+        a = O.bf16(A).T if ta else O.bf16(A)
+        b = O.bf16(B).T if tb else O.bf16(B)
+        assert_bf16(f64(C), O.matmul(a, b), f"random gemm {M}x{N}x{K} ta={ta} tb={tb} cta{cg}")
