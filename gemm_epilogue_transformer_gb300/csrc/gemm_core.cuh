@@ -618,19 +618,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
           Epi::chunk(st, ep, cx, cs, acc, pre, in, box0, box1);
-          if constexpr (kIn > 0) {
-            if (in) {
-              // every lane has read the slot: order those reads before the TMA
-              // write that refills it
-              fence_proxy_async_smem();
-              __syncwarp();
-              ++seq_used;
-              if (lane == 0) issue_ahead();
-            }
-          }
-          if (nslots > 0 && (cs % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1) {
+          // One proxy fence and warp sync serve both hand-offs to TMA: every
+          // lane's reads of the input slot happen before the copy that refills
+          // it, and every lane's staging writes before the store that reads them.
+          const bool store_step = nslots > 0 && (cs % Epi::kChunksPerStore) == Epi::kChunksPerStore - 1;
+          if (in != 0 || store_step) {
             fence_proxy_async_smem();
             __syncwarp();
+          }
+          if (store_step) {
             if (lane == 0) {
               for (int s = 0; s < nslots; ++s) {
                 int map, x, y;
@@ -640,6 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_commit();
             }
             if constexpr (C::kStageBufs == 2) sbuf ^= 1;
+          }
+          if constexpr (kIn > 0) {
+            if (in) {
+              ++seq_used;
+              if (lane == 0) issue_ahead();
+            }
           }
         };
         // vector operands: chunk c+1's loads are issued before chunk c runs
