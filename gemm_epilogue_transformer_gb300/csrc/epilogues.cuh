@@ -291,36 +291,57 @@ struct EpiSwiGLUBwd {
 // kScale: the delayed RMSNorm row scale of the block chain, out = RoPE(r[i] *
 // acc) (CODA note, Key design 1 composed with Key design 2; the row scale
 // commutes with the per-row rotation).
+//
+// Table traffic. A warp's 32 rows are positions p0 + l, l = 0..31. When S is a
+// multiple of 32 (no wrap inside a warp) and head_dim <= 128, the angle of
+// position p0 + l is the sum of the angles of p0 and of l, so
+//   cos((p0+l) w) = cos(p0 w) cos(l w) - sin(p0 w) sin(l w),
+//   sin((p0+l) w) = sin(p0 w) cos(l w) + cos(p0 w) sin(l w).
+// Table rows 0..31 (the l factors) are copied into shared memory once per CTA;
+// per chunk a warp reads only row p0's 16 cos and 16 sin values (one broadcast
+// load each). That replaces 4 KiB of table reads per warp and chunk from L2 by
+// 128 bytes. Otherwise each row loads its own 16 + 16 values directly.
+// Requires tables of angles linear in the position, cos_tab[p, i] =
+// cos(p * w_i), as coda_rope_tables writes them.
 template <int kSign, bool kScale = false>
 struct EpiRope {
   struct Params {
     const float* cos_tab;
     const float* sin_tab;
     int S, head_dim, rope_cols;
-    int tma_tables;  // 1: the cos/sin slices arrive by TMA (S % 32 == 0); 0: direct loads
-    const float* r;  // kScale only
+    int lane_tables;  // 1: angle addition with table rows 0..31 in shared memory; 0: per-row loads
+    const float* r;   // kScale only
   };
   struct State {
     float rv;
   };
+  // lane_tables: row p0's values (the same for the whole warp); else the row's own
   struct Pre {
     uint4 c[4], s[4];
   };
-  // With S % 32 == 0 a warp's 32 rows are 32 consecutive positions, so the
-  // chunk's 16 cos and 16 sin columns are one 32 x 64B fp32 box each.
-  static constexpr int kInBoxes = 2;
-  __device__ static bool has_input(const Params& ep, const EpiCtx& cx, int c) {
-    return ep.tma_tables && cx.n0 + 32 * c < ep.rope_cols;
+  CODA_NO_INPUT
+  // Table rows 0..31 of cos and sin, 256 bytes per row (64 frequencies at
+  // most); 16-byte granule j of row l sits at granule j ^ (l & 7), so the
+  // warp's 32 row reads of one granule are conflict-free.
+  static constexpr int kSharedBytes = 2 * 32 * 256;
+  __device__ static uint32_t lane_addr(uint32_t base, int t, int l, int j) {
+    return base + t * (32 * 256) + l * 256 + ((j ^ (l & 7)) << 4);
   }
-  __device__ static void in_coord(const Params& ep, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
-    map = b;
-    x = ((cx.n0 + 32 * c) % ep.head_dim) >> 1;
-    y = cx.wrow0 % ep.S;
+  __device__ static void init_shared(const Params& ep, uint32_t base, int tid) {
+    if (!ep.lane_tables) return;
+    const int g = ep.head_dim >> 3;  // 16-byte granules per table row (head_dim / 2 floats)
+    for (int idx = tid; idx < 2 * 32 * g; idx += 128) {
+      const int t = idx / (32 * g), rem = idx - t * 32 * g;
+      const int l = rem / g, j = rem - l * g;
+      const float* src = (t ? ep.sin_tab : ep.cos_tab) + static_cast<long>(l) * (ep.head_dim >> 1) + 4 * j;
+      const uint4 v = ldg_nc_v4(src);
+      st_shared_v4(lane_addr(base, t, l, j), v.x, v.y, v.z, v.w);
+    }
   }
   __device__ static void prefetch(const Params& ep, const EpiCtx& cx, int c, Pre& pr) {
     const int col0 = cx.n0 + 32 * c;
-    if (!ep.tma_tables && col0 < ep.rope_cols) {
-      const int pos = (cx.row < cx.M) ? (cx.row % ep.S) : 0;
+    if (col0 < ep.rope_cols) {
+      const int pos = ep.lane_tables ? (cx.wrow0 % ep.S) : ((cx.row < cx.M) ? (cx.row % ep.S) : 0);
       const int half = ep.head_dim >> 1;
       const int i0 = (col0 % ep.head_dim) >> 1;
       const float* cp = ep.cos_tab + static_cast<long>(pos) * half + i0;
@@ -332,18 +353,14 @@ struct EpiRope {
       }
     }
   }
-  // One store box per chunk, and a one-chunk table ring (the slices are L2
-  // resident): the shared memory saved buys a sixth mainloop stage, which
-  // measured 1.7 % faster than five stages with a two-chunk ring.
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 1;
-  static constexpr int kInRingBytes = 4096;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
-                               uint32_t in, uint32_t box0, uint32_t) {
+                               uint32_t, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
     if constexpr (kScale) {
 #pragma unroll
@@ -351,29 +368,35 @@ struct EpiRope {
     }
     if (col0 < ep.rope_cols) {
       float cs[16], sn[16];
-      uint4 tc[4], ts[4];
-      if (in) {
-        box_row(in, cx.lane, tc);
-        box_row(in + kInBoxBytes, cx.lane, ts);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tc[q] = pr.c[q];
-          ts[q] = pr.s[q];
-        }
-      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 a = tc[q];
-        const uint4 b = ts[q];
-        cs[4 * q + 0] = __uint_as_float(a.x);
-        cs[4 * q + 1] = __uint_as_float(a.y);
-        cs[4 * q + 2] = __uint_as_float(a.z);
-        cs[4 * q + 3] = __uint_as_float(a.w);
-        sn[4 * q + 0] = __uint_as_float(b.x);
-        sn[4 * q + 1] = __uint_as_float(b.y);
-        sn[4 * q + 2] = __uint_as_float(b.z);
-        sn[4 * q + 3] = __uint_as_float(b.w);
+        cs[4 * q + 0] = __uint_as_float(pr.c[q].x);
+        cs[4 * q + 1] = __uint_as_float(pr.c[q].y);
+        cs[4 * q + 2] = __uint_as_float(pr.c[q].z);
+        cs[4 * q + 3] = __uint_as_float(pr.c[q].w);
+        sn[4 * q + 0] = __uint_as_float(pr.s[q].x);
+        sn[4 * q + 1] = __uint_as_float(pr.s[q].y);
+        sn[4 * q + 2] = __uint_as_float(pr.s[q].z);
+        sn[4 * q + 3] = __uint_as_float(pr.s[q].w);
+      }
+      if (ep.lane_tables) {
+        // (cs, sn) hold row p0's values: add the angle of this lane's offset
+        const int j0 = ((col0 % ep.head_dim) >> 1) >> 2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 lc = ld_shared_v4(lane_addr(cx.shared, 0, cx.lane, j0 + q));
+          const uint4 ls = ld_shared_v4(lane_addr(cx.shared, 1, cx.lane, j0 + q));
+          const float cl[4] = {__uint_as_float(lc.x), __uint_as_float(lc.y), __uint_as_float(lc.z),
+                               __uint_as_float(lc.w)};
+          const float sl[4] = {__uint_as_float(ls.x), __uint_as_float(ls.y), __uint_as_float(ls.z),
+                               __uint_as_float(ls.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float cb = cs[4 * q + e], sb = sn[4 * q + e];
+            cs[4 * q + e] = cb * cl[e] - sb * sl[e];
+            sn[4 * q + e] = sb * cl[e] + cb * sl[e];
+          }
+        }
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k) {

@@ -26,13 +26,11 @@ int coda_gemm_rowscale_rope(int M, int N, int K, const coda_bf16* X, const coda_
   CODA_REQ_PTR16(cos_tab);
   CODA_REQ_PTR16(sin_tab);
   CODA_REQ_PTR16(out);
-  CUtensorMap o, tc, ts;
+  CUtensorMap o;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  const int tma = S % 32 == 0;
-  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
   using E = EpiRope<1, true>;
-  E::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma, r};
-  return launch_fused<E>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, tc, ts, ep, as_stream(stream));
+  E::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, rope_lane_tables(S, head_dim), r};
+  return launch_fused<E>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 int coda_gemm_rowscale_swiglu(int M, int F, int K, const coda_bf16* X, const coda_bf16* Wgu, const float* r,

@@ -60,7 +60,7 @@ constexpr int kMaxInSlots = 4;
 // The mainloop gets as many stages as the shared memory left after the
 // epilogue's staging and input ring allows, at most 6 (pair) or 4 (single):
 // 6 / 4 without inputs, 5 / 3 with an 8 KiB ring or three staging boxes.
-template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes, int kBufs = kEpiBufs>
+template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes, int kBufs = kEpiBufs, int kShared = 0>
 struct Cfg {
   static constexpr int kPair = kCG == 1 ? 1 : 2;  // CTAs per MMA (cta_group)
   static constexpr int kPairs = kCG / kPair;       // MMA groups per cluster (1, or 2 sharing A)
@@ -74,21 +74,23 @@ struct Cfg {
   static constexpr int kEpiWarpBytes = kStageBoxBytes * kSlots * kBufs;
   static constexpr int kInSlots = kIn ? kInWarp / (kIn * kInBoxBytes) : 0;
   static constexpr int kInBytes = kIn ? kEpiWarps * kInWarp : 0;
+  static constexpr int kSharedBytes = kShared;  // epilogue-wide table, filled once per CTA
   // As many mainloop stages as the rest of shared memory leaves room for, at
   // most 6 (SM pair) or 4 (single SM).
-  static constexpr int kFixedBytes = 1024 + kEpiWarps * kEpiWarpBytes + kInBytes + 16 +
+  static constexpr int kFixedBytes = 1024 + kEpiWarps * kEpiWarpBytes + kInBytes + kShared + 16 +
                                      8 * (2 + 2 + 1 + kEpiWarps * kMaxInSlots);
   static constexpr int kFitStages = (232448 - kFixedBytes) / (kStageBytes + 16);
   static constexpr int kMaxStages = kCG >= 2 ? 6 : 4;
   static constexpr int kStages = kFitStages < kMaxStages ? kFitStages : kMaxStages;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kNumBars * 8 + 16;
+      1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kShared + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStages >= 3, "mainloop ring");
   static_assert(kInSlots <= kMaxInSlots && (kIn == 0 || kInSlots >= 1), "input ring slots");
   static_assert(kSlots >= 1 && kSlots <= 3, "staging slots");
   static_assert(kBufs == 1 || kBufs == 2, "staging buffers");
+  static_assert(kShared % 16 == 0, "epilogue table alignment");
 };
 
 // Per-epilogue staging buffers: two unless the epilogue declares kStageBufs.
@@ -111,6 +113,22 @@ template <class E>
 struct InRingOf<E, std::void_t<decltype(E::kInRingBytes)>> {
   static constexpr int value = E::kInRingBytes;
 };
+
+// Per-epilogue shared table: none unless the epilogue declares kSharedBytes,
+// in which case its init_shared() fills the table once per CTA before the
+// first tile (all four epilogue warps, then a named barrier among them).
+template <class E, class = void>
+struct SharedOf {
+  static constexpr int value = 0;
+};
+template <class E>
+struct SharedOf<E, std::void_t<decltype(E::kSharedBytes)>> {
+  static constexpr int value = E::kSharedBytes;
+};
+
+template <class Epi, int kCG>
+using CfgOf = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value,
+                  SharedOf<Epi>::value>;
 
 constexpr int BSEG = 128;  // epilogue segment: columns per partial-statistics block
 
@@ -140,6 +158,7 @@ struct EpiCtx {
   int ew;     // warp quarter (TMEM lanes 32*ew .. 32*ew+31)
   int lane;
   int k_blocks;
+  uint32_t shared;  // shared-memory address of the epilogue's table (kSharedBytes), 0 if none
 };
 
 // Tile order: groups of group_m row-blocks sweep all column blocks, so the
@@ -300,12 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const GemmShape p, const typename Epi::Params ep) {
   constexpr int kIn = Epi::kInBoxes;
   constexpr int kSlots = Epi::kMaxSlots;
-  using C = Cfg<kCG, kIn, kSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value>;
+  using C = CfgOf<Epi, kCG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_epi = smem + C::kStages * C::kStageBytes;
   uint8_t* s_in = s_epi + kEpiWarps * C::kEpiWarpBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_in + C::kInBytes);
+  uint8_t* s_tab = s_in + C::kInBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_tab + C::kSharedBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -540,6 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so load latency overlaps TMEM reads, math and the mainloop.
     const int ew = warp & 3;
     const uint32_t my_stage = smem_u32(s_epi) + ew * C::kEpiWarpBytes;
+    if constexpr (C::kSharedBytes > 0) {
+      // the 128 epilogue threads fill the table together, then wait for each other
+      Epi::init_shared(ep, smem_u32(s_tab), static_cast<int>(threadIdx.x) - 64);
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
     // Segment `seg` (128 columns) of work item tt; false if it lies past N.
     auto make_ctx = [&](int tt, int seg, EpiCtx& cx) {
       int n0, ncols;
@@ -555,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cx.wrow0 = cx.m0 + 32 * ew;
       cx.row = cx.wrow0 + lane;
       cx.k_blocks = p.k_blocks;
+      cx.shared = C::kSharedBytes ? smem_u32(s_tab) : 0u;
       return cx.n0 < p.N;
     };
     auto item_segs = [&](int tt) { return tt < p.full_items ? BN / BSEG : 1; };

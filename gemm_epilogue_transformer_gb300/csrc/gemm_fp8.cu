@@ -54,12 +54,10 @@ int coda_gemm_rope_fp8(int M, int N, int K, const uint8_t* X, const uint8_t* W, 
   CODA_REQ_PTR16(cos_tab);
   CODA_REQ_PTR16(sin_tab);
   CODA_REQ_PTR16(out);
-  CUtensorMap o, tc, ts;
+  CUtensorMap o;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  const int tma = S % 32 == 0;
-  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
-  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma, nullptr};
-  return launch_fused<EpiRope<1>, true>(fn, M, N, K, X, K, 0, W, K, 0, o, o, tc, ts, ep, as_stream(stream), alpha);
+  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, rope_lane_tables(S, head_dim), nullptr};
+  return launch_fused<EpiRope<1>, true>(fn, M, N, K, X, K, 0, W, K, 0, o, o, o, o, ep, as_stream(stream), alpha);
 }
 
 int coda_gemm_swiglu_fp8(int M, int F, int K, const uint8_t* X, const uint8_t* Wgu, float alpha, coda_bf16* A_out,

@@ -116,12 +116,10 @@ int coda_gemm_rope(int M, int N, int K, const coda_bf16* X, const coda_bf16* W, 
   const char* fn = "coda_gemm_rope";
   int rc = rope_common(fn, M, N, K, X, W, cos_tab, sin_tab, S, head_dim, rope_cols, out);
   if (rc || M == 0 || N == 0) return rc;
-  CUtensorMap o, tc, ts;
+  CUtensorMap o;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  const int tma = S % 32 == 0;
-  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
-  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma};
-  return launch_fused<EpiRope<1>>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, tc, ts, ep, as_stream(stream));
+  EpiRope<1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, rope_lane_tables(S, head_dim)};
+  return launch_fused<EpiRope<1>>(fn, M, N, K, X, K, 0, W, N, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16* B, const float* cos_tab,
@@ -130,12 +128,10 @@ int coda_gemm_rope_bwd(int M, int N, int K, const coda_bf16* A, const coda_bf16*
   const char* fn = "coda_gemm_rope_bwd";
   int rc = rope_common(fn, M, N, K, A, B, cos_tab, sin_tab, S, head_dim, rope_cols, out);
   if (rc || M == 0 || N == 0) return rc;
-  CUtensorMap o, tc, ts;
+  CUtensorMap o;
   if ((rc = make_out_map(&o, out, M, N, N))) return rc;
-  const int tma = S % 32 == 0;
-  if ((rc = rope_table_maps(tma, cos_tab, sin_tab, S, head_dim, o, &tc, &ts))) return rc;
-  EpiRope<-1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, tma};
-  return launch_fused<EpiRope<-1>>(fn, M, N, K, A, K, 0, B, N, /*b_mn=*/1, o, o, tc, ts, ep, as_stream(stream));
+  EpiRope<-1>::Params ep{cos_tab, sin_tab, S, head_dim, rope_cols, rope_lane_tables(S, head_dim)};
+  return launch_fused<EpiRope<-1>>(fn, M, N, K, A, K, 0, B, N, /*b_mn=*/1, o, o, o, o, ep, as_stream(stream));
 }
 
 }  // extern "C"

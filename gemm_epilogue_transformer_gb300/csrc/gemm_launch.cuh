@@ -31,21 +31,11 @@ inline int check_fused(const char* fn, int M, int N, int K, const void* A, const
   return CODA_OK;
 }
 
-// TMA maps over the fp32 cos/sin tables [S, head_dim/2]: 32 positions x 16
-// frequencies (64 bytes) per box. Used when S % 32 == 0, so that a warp's 32
-// rows never wrap inside a box; otherwise the epilogue loads the tables directly.
-inline int rope_table_maps(int tma, const float* c, const float* s, int S, int head_dim, const CUtensorMap& other,
-                           CUtensorMap* tc, CUtensorMap* ts) {
-  if (!tma) {
-    *tc = other;
-    *ts = other;
-    return CODA_OK;
-  }
-  const uint64_t half = static_cast<uint64_t>(head_dim / 2);
-  int rc = make_map_f32(tc, c, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (rc) return rc;
-  return make_map_f32(ts, s, half, static_cast<uint64_t>(S), half * 4u, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-}
+// The RoPE epilogue forms a warp's cos/sin values by angle addition from table
+// rows 0..31 (kept in shared memory) and the warp's first position when S is a
+// multiple of 32 (a warp's 32 rows never wrap) and a table row fits 256 bytes
+// (head_dim <= 128); otherwise every row loads its own values.
+inline int rope_lane_tables(int S, int head_dim) { return (S % 32 == 0 && head_dim <= 128) ? 1 : 0; }
 
 // kF8: E4M3 operands, K-major only (A [M, K], B stored [N, K], lda / ldb in
 // bytes = elements), 128-element K stages, accumulator scaled by alpha.
@@ -54,7 +44,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
                    const void* B, int ldb, int b_mn, const CUtensorMap& o0, const CUtensorMap& o1,
                    const CUtensorMap& i0, const CUtensorMap& i1, const typename Epi::Params& ep,
                    cudaStream_t stream, float alpha = 1.0f) {
-  using C = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value>;
+  using C = CfgOf<Epi, kCG>;
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));

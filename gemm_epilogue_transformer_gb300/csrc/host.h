@@ -57,8 +57,5 @@ int make_map_bf16_mn3d(CUtensorMap* m, const void* base, uint64_t mn, uint64_t k
 // The same for a byte array (FP8 operands).
 int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
-// The same for an fp32 array.
-int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 }  // namespace coda

@@ -153,11 +153,6 @@ int make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
   return make_map(CU_TENSOR_MAP_DATA_TYPE_UINT8, m, base, inner, outer, row_bytes, box_inner, box_outer, sw);
 }
 
-int make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  return make_map(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, base, inner, outer, row_bytes, box_inner, box_outer, sw);
-}
-
 }  // namespace coda
 
 using namespace coda;

@@ -72,13 +72,14 @@ def _fp8_case(coda):
     return run, ref
 
 
-@pytest.mark.parametrize("case", [_rope_case, _swiglu_bwd_case, _fp8_case], ids=["rope_tma_tables", "swiglu_bwd_inputs",
-                                                                             "fp8_mainloop"])
+@pytest.mark.parametrize("case", [_rope_case, _swiglu_bwd_case, _fp8_case],
+                         ids=["rope_shared_tables", "swiglu_bwd_inputs", "fp8_mainloop"])
 @pytest.mark.parametrize("cg", [1, 2, 4], ids=["cta1", "cta2", "cta4"])
 def test_abort_with_epilogue_inputs_in_flight(coda, cg, case):
-    """The same missing fill in kernels whose epilogue warps already have TMA
-    input boxes in flight (RoPE tables, SwiGLU pre-activations) and in the FP8
-    mainloop: the abort path drains them, and the context stays usable."""
+    """The same missing fill in a kernel whose epilogue warps filled a shared
+    table first (RoPE), in one whose epilogue warps already have TMA input
+    boxes in flight (SwiGLU pre-activations), and in the FP8 mainloop: the
+    abort path drains what is in flight, and the context stays usable."""
     run, ref = case(coda)
     try:
         coda.coda_set_cta_group(cg)

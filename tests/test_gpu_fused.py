@@ -154,7 +154,10 @@ def test_swiglu_fwd_bwd(coda, M, K, F):
 @pytest.mark.parametrize("M,K,N,hd,rope_cols,S", [
     (300, 200, 768, 128, 512, 256),   # positions wrap (row mod S), V columns pass through
     (256, 512, 1536, 128, 1024, 4096),
-    (130, 72, 320, 64, 256, 100),
+    (130, 72, 320, 64, 256, 100),     # S % 32 != 0: every row loads its own table values
+    (192, 96, 576, 96, 384, 96),      # 12 table granules per row (swizzled shared copy)
+    (160, 64, 256, 32, 128, 64),      # the smallest head
+    (200, 128, 1024, 256, 512, 512),  # head_dim > 128: rows load their own values
 ])
 def test_rope_fwd_bwd(coda, M, K, N, hd, rope_cols, S):
     theta = 10000.0
