@@ -43,7 +43,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
 constexpr int kStageBoxBytes = 32 * 64;  // one epilogue TMA store box: 32 rows x 64 bytes
 constexpr int kEpiBufs = 2;              // staging double buffer
-// Rank-2 epilogue inputs (z, Y, h1, GU, RoPE tables) arrive by TMA in 32 x 64B
+// Rank-2 epilogue inputs (z, Y, h1, dres, GU) arrive by TMA in 32 x 64B
 // boxes into a per-warp ring of kInWarpBytes, issued several chunks ahead.
 constexpr int kInBoxBytes = 32 * 64;
 constexpr int kInWarpBytes = 8192;

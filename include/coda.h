@@ -161,7 +161,12 @@ int coda_rope_tables(int S, int head_dim, double theta, float* cos_out, float* s
  *   out_e = a_e cos - a_o sin, out_o = a_e sin + a_o cos; columns at or
  *   beyond rope_cols (V) pass through.
  *   X [M,K], W [K,N], cos/sin [S, head_dim/2] fp32 -> out [M,N] bf16.
- *   head_dim a multiple of 32, rope_cols a multiple of head_dim and <= N. */
+ *   head_dim a multiple of 32, rope_cols a multiple of head_dim and <= N.
+ *   The tables must hold angles linear in the position, cos_tab[p, i] =
+ *   cos(p w_i) and sin_tab likewise, as coda_rope_tables writes them: when S
+ *   is a multiple of 32 and head_dim <= 128 the kernel forms the values of
+ *   positions p0 + l (l < 32, p0 a multiple of 32) by angle addition from
+ *   table rows p0 and l. (The same holds for every RoPE epilogue below.) */
 int coda_gemm_rope(int M, int N, int K, const coda_bf16* X, const coda_bf16* W, const float* cos_tab,
                    const float* sin_tab, int S, int head_dim, int rope_cols, coda_bf16* out, coda_stream_t stream);
 
