@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -172,9 +173,14 @@ ROPE_KERNEL_SOURCES = ("ptx.cuh", "gemm_core.cuh", "epilogues.cuh", "gemm_launch
 
 
 def kernel_src_hash():
+    """Hash of the RoPE kernel's sources with comments and blank space removed,
+    so that a comment edit does not void the recorded ncu traffic."""
     h = hashlib.sha256()
     for f in ROPE_KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "gemm_epilogue_transformer_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "gemm_epilogue_transformer_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
