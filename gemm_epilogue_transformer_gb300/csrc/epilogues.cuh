@@ -24,8 +24,12 @@ __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.
 // Shared-memory trade: an epilogue may declare kStageBufs = 1 (single-buffered
 // store staging), kInRingBytes = 4096 (a smaller input ring) or kMaxSlots = 1
 // (one store box per chunk). Each frees room for a sixth mainloop stage on SM
-// pairs; measured 1.5-3.5 % faster for every epilogue with inputs and for
+// pairs; measured 1.5-3.5 % faster for the one-box input epilogues and for
 // SwiGLU with its GU side output than five stages with the larger buffers.
+// The two-box input epilogues (SwiGLU backward, RMSNorm backward with the
+// residual gradient) keep two chunks of inputs in flight (8 KiB) and five
+// stages instead: with one chunk in flight each chunk waits a full HBM round
+// trip, and at K = 2048 the SwiGLU backward ran 12 % slower.
 
 // Epilogues without global inputs carry an empty prefetch buffer.
 struct NoPre {
@@ -254,7 +258,7 @@ struct EpiSwiGLUBwd {
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   static constexpr int kStageBufs = 1;
-  static constexpr int kInRingBytes = 4096;
+  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
@@ -660,7 +664,7 @@ struct EpiSwiGLUBwdRowdot {
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   static constexpr int kStageBufs = 1;
-  static constexpr int kInRingBytes = 4096;
+  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = 0.f;
@@ -731,7 +735,7 @@ struct EpiRmsNormBwdRes {
   }
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 1;
-  static constexpr int kInRingBytes = 4096;
+  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     if (cx.row < cx.M) {
