@@ -27,9 +27,12 @@ __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.
 // pairs; measured 1.5-3.5 % faster for the one-box input epilogues and for
 // SwiGLU with its GU side output than five stages with the larger buffers.
 // The two-box input epilogues (SwiGLU backward, RMSNorm backward with the
-// residual gradient) keep two chunks of inputs in flight (8 KiB) and five
-// stages instead: with one chunk in flight each chunk waits a full HBM round
-// trip, and at K = 2048 the SwiGLU backward ran 12 % slower.
+// residual gradient) take the ring size as a template argument: 4096 bytes
+// (one chunk of inputs in flight, six stages) or 8192 (two chunks, five
+// stages). With one chunk in flight each chunk waits a full HBM round trip,
+// which a short mainloop cannot hide: at K = 2048 the SwiGLU backward ran 14 %
+// slower with the small ring, at K = 4096 2 % faster. The launchers pick by K
+// (gemm_launch.cuh, kDeepRingMaxK).
 
 // Epilogues without global inputs carry an empty prefetch buffer.
 struct NoPre {
@@ -241,6 +244,7 @@ struct EpiSwiGLU {
 // acc = dA[:, f0..f0+31]; loads the saved GU pairs, recomputes sigmoid(G), and
 // emits interleaved (dG, dU) for 64 output columns: two store boxes.
 // (pith page, Figure 7: one incoming gradient -> both paired input gradients.)
+template <int kRing = 4096>
 struct EpiSwiGLUBwd {
   struct Params {
     const __nv_bfloat16* gu;  // [M, 2F]
@@ -258,7 +262,7 @@ struct EpiSwiGLUBwd {
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   static constexpr int kStageBufs = 1;
-  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
+  static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
@@ -644,6 +648,7 @@ struct EpiRmsNormBwd {
 // times the loaded bf16 GU), and the output stored already row-scaled,
 // dGUr = r (.)row dGU, the form both consumers take (the weight gradient
 // h2g^T dGUr and the RMSNorm-backward GEMM on dGUr Wgu^T = r (.)row G).
+template <int kRing = 4096>
 struct EpiSwiGLUBwdRowdot {
   struct Params {
     const __nv_bfloat16* gu;  // [M, 2F]
@@ -664,7 +669,7 @@ struct EpiSwiGLUBwdRowdot {
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   static constexpr int kStageBufs = 1;
-  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
+  static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = 0.f;
@@ -708,6 +713,7 @@ struct EpiSwiGLUBwdRowdot {
 // row-scaled gradient). dh = gamma (.) Gr - r^2 s h + dres, where dres is the
 // gradient reaching h through the residual connection (a second input tile);
 // column partial of Gr h (= r G h) over the warp's 32 rows.
+template <int kRing = 4096>
 struct EpiRmsNormBwdRes {
   struct Params {
     const __nv_bfloat16* h;
@@ -735,7 +741,7 @@ struct EpiRmsNormBwdRes {
   }
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 1;
-  static constexpr int kInRingBytes = 8192;  // two chunks of input boxes in flight
+  static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     if (cx.row < cx.M) {

@@ -19,9 +19,14 @@ int coda_gemm_swiglu_bwd(int M, int F, int K, const coda_bf16* dY, const coda_bf
   if ((rc = make_out_map(&o, dgu_out, M, 2 * F, 2 * F))) return rc;
   CUtensorMap ig;
   if ((rc = make_out_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
-  EpiSwiGLUBwd::Params ep{reinterpret_cast<const __nv_bfloat16*>(gu)};
+  const auto* g = reinterpret_cast<const __nv_bfloat16*>(gu);
   // dA = dY Wd^T: Wd is stored [F, K] = [N, K], a K-major B operand.
-  return launch_fused<EpiSwiGLUBwd>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, ep, as_stream(stream));
+  if (K <= kDeepRingMaxK) {
+    using E = EpiSwiGLUBwd<8192>;
+    return launch_fused<E>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, E::Params{g}, as_stream(stream));
+  }
+  using E = EpiSwiGLUBwd<>;
+  return launch_fused<E>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, E::Params{g}, as_stream(stream));
 }
 
 int coda_gemm_rowdot(int M, int N, int K, const coda_bf16* dO, const coda_bf16* Wn, const coda_bf16* Y,

@@ -71,10 +71,16 @@ int coda_gemm_swiglu_bwd_rowdot(int M, int F, int K, const coda_bf16* dY, const 
   CUtensorMap o, ig;
   if ((rc = make_out_map(&o, dgur_out, M, 2 * F, 2 * F))) return rc;
   if ((rc = make_out_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
-  EpiSwiGLUBwdRowdot::Params ep{reinterpret_cast<const __nv_bfloat16*>(gu), r, pdot_out};
+  const auto* g = reinterpret_cast<const __nv_bfloat16*>(gu);
   // dA = dY Wd^T: Wd is stored [F, K] = [N, K], a K-major B operand.
-  return launch_fused<EpiSwiGLUBwdRowdot>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, ep,
-                                          as_stream(stream));
+  if (K <= kDeepRingMaxK) {
+    using E = EpiSwiGLUBwdRowdot<8192>;
+    return launch_fused<E>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, E::Params{g, r, pdot_out},
+                           as_stream(stream));
+  }
+  using E = EpiSwiGLUBwdRowdot<>;
+  return launch_fused<E>(fn, M, F, K, dY, K, 0, Wd, K, /*b_mn=*/0, o, o, ig, ig, E::Params{g, r, pdot_out},
+                         as_stream(stream));
 }
 
 int coda_gemm_rmsnorm_bwd_res(int M, int d, int K, const coda_bf16* dYr, const coda_bf16* W1, const coda_bf16* h,
@@ -95,11 +101,17 @@ int coda_gemm_rmsnorm_bwd_res(int M, int d, int K, const coda_bf16* dYr, const c
   if ((rc = make_out_map(&o, dh_out, M, d, d))) return rc;
   if ((rc = make_out_map(&ih, h, M, d, d))) return rc;
   if ((rc = make_out_map(&ir, dres, M, d, d))) return rc;
-  EpiRmsNormBwdRes::Params ep{reinterpret_cast<const __nv_bfloat16*>(h), reinterpret_cast<const __nv_bfloat16*>(gamma),
-                              r, s, pdg_out};
+  const auto* hb = reinterpret_cast<const __nv_bfloat16*>(h);
+  const auto* gb = reinterpret_cast<const __nv_bfloat16*>(gamma);
   // Gr = dYr W1^T: W1 is stored [d, K] = [N, K], a K-major B operand.
-  return launch_fused<EpiRmsNormBwdRes>(fn, M, d, K, dYr, K, 0, W1, K, /*b_mn=*/0, o, o, ih, ir, ep,
-                                        as_stream(stream));
+  if (K <= kDeepRingMaxK) {
+    using E = EpiRmsNormBwdRes<8192>;
+    return launch_fused<E>(fn, M, d, K, dYr, K, 0, W1, K, /*b_mn=*/0, o, o, ih, ir, E::Params{hb, gb, r, s, pdg_out},
+                           as_stream(stream));
+  }
+  using E = EpiRmsNormBwdRes<>;
+  return launch_fused<E>(fn, M, d, K, dYr, K, 0, W1, K, /*b_mn=*/0, o, o, ih, ir, E::Params{hb, gb, r, s, pdg_out},
+                         as_stream(stream));
 }
 
 }  // extern "C"

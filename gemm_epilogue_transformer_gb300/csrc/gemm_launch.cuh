@@ -11,6 +11,10 @@
 namespace coda {
 
 constexpr int kGroupM = 16;  // 128-row blocks per raster group
+// Two-box input epilogues keep two chunks of inputs in flight (a larger ring,
+// one mainloop stage less) when K is at most this: a mainloop that short
+// cannot hide one HBM round trip per chunk.
+constexpr int kDeepRingMaxK = 3072;
 
 // Output map for a TMA store target: row-major bf16 [rows, cols], leading
 // dimension ld (elements), 32 x 32 boxes with the 64-byte swizzle.
