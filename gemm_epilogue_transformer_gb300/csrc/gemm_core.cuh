@@ -382,6 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kCG >= 2) cluster_sync_all();  // barriers of all CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above (barriers, TMEM, tensor-map prefetch) touches no global
+  // memory, so it may overlap the previous kernel of the stream; everything
+  // below reads or writes global memory and waits for that kernel first.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (every CTA)

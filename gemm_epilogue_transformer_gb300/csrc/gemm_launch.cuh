@@ -87,7 +87,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   if (dev < 0 || dev >= 64) return fail(CODA_ERR_INVALID, "%s: device index %d", fn, dev);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCG;
   attr[0].val.clusterDim.y = 1;
@@ -141,6 +141,12 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
 
   const int clusters = p.num_items < cmax ? p.num_items : cmax;
   cfg.gridDim = dim3(clusters * kCG, 1, 1);
+  // Programmatic dependent launch: the grid may be scheduled while the previous
+  // kernel of the stream drains; the kernel waits for it before any global
+  // access (griddep_wait), so only launch latency and the prologue overlap.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tA, tB, o0, o1, i0, i1, p, ep);
   if (e != cudaSuccess) return fail_cuda(e, fn);
   e = cudaGetLastError();
