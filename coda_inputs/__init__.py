@@ -143,6 +143,27 @@ def rms_chain(M: int, K: int, d: int, N2: int, seed: int = 0, bwd_K: int | None 
     return out
 
 
+def rms_chain_outliers(M: int, K: int, d: int, N2: int, seed: int = 0, frac: float = 0.01,
+                       scale: float = 20.0) -> dict:
+    """The rms_chain problem with outlier channels in the residual stream: a
+    `frac` share of the d channels of z (chosen by the seed) is drawn `scale`
+    times wider, a synthetic stand-in for the few large-magnitude channels of
+    trained models' residual streams. Same spawn order as rms_chain, plus one
+    child for the channel choice."""
+    g = _children(seed, 8)
+    z = g[2].standard_normal(size=(M, d), dtype=np.float32)
+    cols = g[7].choice(d, size=max(1, int(round(frac * d))), replace=False)
+    z[:, cols] *= np.float32(scale)
+    return {
+        "x": normal_bf16(g[0], (M, K)),
+        "W0": normal_bf16(g[1], (K, d), std=1.0 / np.sqrt(K)),
+        "z": f32_to_bf16_bits(z),
+        "gamma": normal_bf16(g[3], (d,), std=0.1, mean=1.0),
+        "W1": normal_bf16(g[4], (d, N2), std=1.0 / np.sqrt(d)),
+        "outlier_cols": np.sort(cols),
+    }
+
+
 def rope_problem(M: int, K: int, N3: int, seed: int = 0, with_bwd: bool = True) -> dict:
     """QKV projection X[M,K] ~ N(0,1) times W[K,N3] ~ N(0,1/K).
 

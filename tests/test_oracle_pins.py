@@ -491,6 +491,23 @@ def test_inputs_bf16_rounding_and_determinism():
     assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
 
 
+def test_outlier_channel_inputs():
+    """The outlier-channel stand-in: the same x, W0, gamma, W1 as rms_chain,
+    and a z whose chosen channels are 20 times wider than the rest."""
+    p = gen.rms_chain_outliers(2048, 32, 400, 16, seed=1, frac=0.01, scale=20.0)
+    q = gen.rms_chain(2048, 32, 400, 16, seed=1)
+    for k in ("x", "W0", "gamma", "W1"):
+        assert np.array_equal(p[k], q[k])
+    cols = p["outlier_cols"]
+    assert len(cols) == 4 and len(set(cols.tolist())) == 4
+    z = O.bf16(p["z"])
+    rest = np.setdiff1d(np.arange(400), cols)
+    assert abs(z[:, rest].std() - 1) < 0.02
+    assert abs(z[:, cols].std() / 20 - 1) < 0.05
+    again = gen.rms_chain_outliers(2048, 32, 400, 16, seed=1, frac=0.01, scale=20.0)
+    assert np.array_equal(again["z"], p["z"])
+
+
 # ---------------------------------------------------------------------------
 # Block-level chain: one period of two GEMM-residual-RMSNorm-GEMM structures
 # (RoPE path, then SwiGLU path). The plain definition is pinned to a torch
