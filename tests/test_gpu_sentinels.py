@@ -146,3 +146,89 @@ def test_every_output_written_once_and_only_inside(coda, cta_group):
     assert L.coda_gemm_ce_bwd(M, V, K, _ptr(A), _ptr(Wv), _ptr(y), _ptr(lse), 1.0 / M, _ptr(dl), st) == 0
     o.check("ce_bwd")
     assert coda.coda_device_status(clear=True) == 0
+
+
+def test_chain_and_fp8_outputs_written_once_and_only_inside(coda, cta_group):
+    """The same sentinel check for the block chain's composed kernels and glue,
+    and for the FP8 mainloop variants."""
+    import torch
+    L = coda.lib()
+    st = torch.cuda.current_stream().cuda_stream
+    g = torch.Generator(device="cuda").manual_seed(23)
+    M, K, d, F = 300, 208, 256, 264
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    r = torch.rand(M, device="cuda", generator=g) + 0.5
+    X = _bf(g, M, K)
+
+    c, s = coda.coda_rope_tables(128, 64, 1e4)
+    W = _bf(g, K, 3 * d, std=K ** -0.5)
+    o = Outs()
+    qkv = o.new(M, 3 * d, bf)
+    assert L.coda_gemm_rowscale_rope(M, 3 * d, K, _ptr(X), _ptr(W), _ptr(r), _ptr(c), _ptr(s), 128, 64, 2 * d,
+                                     _ptr(qkv), st) == 0
+    o.check("rowscale_rope")
+    dqkv = _bf(g, M, 3 * d)
+    o = Outs()
+    dqr, s1 = o.new(M, 3 * d, bf), o.new(M, 1, f32)
+    assert L.coda_rope_bwd_rowdot(M, 3 * d, _ptr(dqkv), _ptr(qkv), _ptr(r), _ptr(c), _ptr(s), 128, 64, 2 * d, d,
+                                  _ptr(dqr), _ptr(s1), st) == 0
+    o.check("rope_bwd_rowdot")
+
+    Wgu = _bf(g, K, 2 * F, std=K ** -0.5)
+    o = Outs()
+    A, GU = o.new(M, F, bf), o.new(M, 2 * F, bf)
+    assert L.coda_gemm_rowscale_swiglu(M, F, K, _ptr(X), _ptr(Wgu), _ptr(r), _ptr(A), _ptr(GU), st) == 0
+    o.check("rowscale_swiglu")
+    gh, Wdn = _bf(g, M, d), _bf(g, F, d, std=d ** -0.5)
+    for Kb in (d, 4096):  # both input-ring instantiations (K <= 3072 and above)
+        ghk, Wdk = (gh, Wdn) if Kb == d else (_bf(g, M, Kb), _bf(g, F, Kb, std=Kb ** -0.5))
+        o = Outs()
+        dgur, pdot = o.new(M, 2 * F, bf), o.new(M, coda.coda_num_col_tiles(F), f32)
+        assert L.coda_gemm_swiglu_bwd_rowdot(M, F, Kb, _ptr(ghk), _ptr(Wdk), _ptr(GU), _ptr(r), _ptr(dgur),
+                                             _ptr(pdot), st) == 0
+        o.check(f"swiglu_bwd_rowdot K={Kb}")
+        W1 = _bf(g, d, 2 * F, std=(2 * F) ** -0.5) if Kb == d else _bf(g, d, Kb, std=Kb ** -0.5)
+        dYr = dgur if Kb == d else _bf(g, M, Kb)
+        h, dres = _bf(g, M, d), _bf(g, M, d)
+        gam = (1 + 0.1 * torch.randn(d, device="cuda", generator=g)).bfloat16()
+        sv = torch.rand(M, device="cuda", generator=g)
+        Kr = 2 * F if Kb == d else Kb
+        o = Outs()
+        dh, pdg = o.new(M, d, bf), o.new(coda.coda_num_row_tiles(M), d, f32)
+        assert L.coda_gemm_rmsnorm_bwd_res(M, d, Kr, _ptr(dYr), _ptr(W1), _ptr(h), _ptr(gam), _ptr(r), _ptr(sv),
+                                           _ptr(dres), _ptr(dh), _ptr(pdg), st) == 0
+        o.check(f"rmsnorm_bwd_res K={Kr}")
+
+    # FP8 (E4M3) mainloop: operands [M,K] and [N,K]; bytes masked away from NaN codes
+    def e4m3(*shape):
+        return torch.randint(0, 256, shape, device="cuda", dtype=torch.uint8, generator=g) & 0x77
+    A8, B8 = e4m3(M, K), e4m3(520, K)
+    o = Outs()
+    C8 = o.new(M, 520, bf)
+    assert L.coda_gemm_fp8(M, 520, K, _ptr(A8), _ptr(B8), 0.01, _ptr(C8), st) == 0
+    o.check("gemm_fp8")
+    o = Outs()
+    R8 = o.new(M, 512, bf)
+    assert L.coda_gemm_rope_fp8(M, 512, K, _ptr(A8), _ptr(B8[:512]), 0.01, _ptr(c), _ptr(s), 128, 64, 256,
+                                _ptr(R8), st) == 0
+    o.check("rope_fp8")
+    o = Outs()
+    A8o, GU8 = o.new(M, F, bf), o.new(M, 2 * F, bf)
+    Wgu8 = e4m3(2 * F, K)
+    assert L.coda_gemm_swiglu_fp8(M, F, K, _ptr(A8), _ptr(Wgu8), 0.01, _ptr(A8o), _ptr(GU8), st) == 0
+    o.check("swiglu_fp8")
+    V = 1000
+    Wv8 = e4m3(V, K)
+    y = torch.randint(0, V, (M,), device="cuda", dtype=i32, generator=g)
+    nbv = coda.coda_num_col_tiles(V)
+    o = Outs()
+    pmax, psum, parg, tgt = o.new(M, nbv, f32), o.new(M, nbv, f32), o.new(M, nbv, i32), o.new(M, 1, f32)
+    assert L.coda_gemm_ce_lse_fp8(M, V, K, _ptr(A8), _ptr(Wv8), 0.01, _ptr(y), _ptr(pmax), _ptr(psum), _ptr(parg),
+                                  _ptr(tgt), st) == 0
+    o.check("ce_lse_fp8")
+    lse = coda.coda_ce_reduce(pmax, psum, parg, tgt[:, 0].contiguous())[0]
+    o = Outs()
+    dl = o.new(M, V, bf)
+    assert L.coda_gemm_ce_bwd_fp8(M, V, K, _ptr(A8), _ptr(Wv8), 0.01, _ptr(y), _ptr(lse), 1.0 / M, _ptr(dl), st) == 0
+    o.check("ce_bwd_fp8")
+    assert coda.coda_device_status(clear=True) == 0
