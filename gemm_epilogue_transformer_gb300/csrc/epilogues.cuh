@@ -15,11 +15,25 @@ namespace coda {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ float exp_f(float x) { return exp2f(x * kLog2e); }
-// 1 / (1 + e^-g) with the fast reciprocal-multiply division (about 2 ulp);
-// for g below about -88 the denominator overflows and the result is 0, the
-// correct limit.
-__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + exp_f(-g)); }
+// e^x = 2^(x log2 e) and 1 / x from the hardware approximations of the PTX
+// ISA (ex2.approx.ftz.f32, rcp.approx.ftz.f32; relative error near 2^-22,
+// far below the bf16 outputs' 2^-9 and the fp32 statistics' 1e-4). Results
+// below the normal range flush to zero, the correct limit for the softmax
+// terms and the sigmoid.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float exp_f(float x) { return ex2_approx(x * kLog2e); }
+// 1 / (1 + e^-g); for g below about -88 the denominator is +inf and the result
+// 0, for g above about 88 it is 1: the correct limits.
+__device__ __forceinline__ float sigmoid_f(float g) { return rcp_approx(1.0f + exp_f(-g)); }
 
 // Shared-memory trade: an epilogue may declare kStageBufs = 1 (single-buffered
 // store staging), kInRingBytes = 4096 (a smaller input ring) or kMaxSlots = 1
