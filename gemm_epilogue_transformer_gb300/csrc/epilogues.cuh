@@ -290,10 +290,12 @@ struct EpiSwiGLUBwd {
       float o[32];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float G = g[2 * k], U = g[2 * k + 1], dA = acc[16 * half + k];
+        // dG = dA U s (1 + G (1 - s)), dU = dA G s, sharing dA s
+        const float G = g[2 * k], U = g[2 * k + 1];
         const float s = sigmoid_f(G);
-        o[2 * k] = dA * U * s * (1.0f + G * (1.0f - s));
-        o[2 * k + 1] = dA * G * s;
+        const float as = acc[16 * half + k] * s;
+        o[2 * k] = (as * U) * fmaf(G, 1.0f - s, 1.0f);
+        o[2 * k + 1] = as * G;
       }
       stage_row32(half ? box1 : box0, cx.lane, o);
     }
@@ -700,14 +702,17 @@ struct EpiSwiGLUBwdRowdot {
       float o[32];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float G = g[2 * k], U = g[2 * k + 1], dA = acc[16 * half + k];
+        // o = r (dG, dU) with dG = dA U s (1 + G (1 - s)), dU = dA G s; the row
+        // dot accumulates on the scaled values and end() divides r out once
+        const float G = g[2 * k], U = g[2 * k + 1];
         const float sg = sigmoid_f(G);
-        const float dG = dA * U * sg * (1.0f + G * (1.0f - sg));
-        const float dU = dA * G * sg;
-        st.dot = fmaf(dG, G, st.dot);
-        st.dot = fmaf(dU, U, st.dot);
-        o[2 * k] = st.rv * dG;
-        o[2 * k + 1] = st.rv * dU;
+        const float as = (acc[16 * half + k] * st.rv) * sg;
+        const float rdG = (as * U) * fmaf(G, 1.0f - sg, 1.0f);
+        const float rdU = as * G;
+        st.dot = fmaf(rdG, G, st.dot);
+        st.dot = fmaf(rdU, U, st.dot);
+        o[2 * k] = rdG;
+        o[2 * k + 1] = rdU;
       }
       stage_row32(half ? box1 : box0, cx.lane, o);
     }
@@ -718,7 +723,8 @@ struct EpiSwiGLUBwdRowdot {
     y = cx.wrow0;
   }
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot;
+    // r > 0 for every row inside M (r = 1 / sqrt(mean + eps))
+    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot / st.rv;
   }
 };
 
