@@ -297,8 +297,14 @@ def main():
     torch.cuda.synchronize(dev)
     G.coda_device_status(clear=True)
 
+    # NVTX ranges name the phases for profilers (ncu --nvtx --nvtx-include "fused/")
+    nvtx = torch.cuda.nvtx
+    nvtx.range_push("fused")
     ms_fused, ms_rope = timed(lambda ev: fused_step(X, W, A, B, ev), a.steps, kernel_events=True)
+    nvtx.range_pop()
+    nvtx.range_push("unfused")
     ms_unfused, _ = timed(lambda ev: unfused_step(), a.steps)
+    nvtx.range_pop()
 
     # End to end through the public API: every step copies its four inputs from
     # pinned host memory to the device, runs the step, and copies its three
@@ -365,9 +371,13 @@ def main():
     e2e_steps = max(3, min(a.steps, 50))
     for _ in range(2):
         e2e_serial_step(None)
+    nvtx.range_push("e2e_serial")
     ms_e2e_serial, _ = timed(e2e_serial_step, e2e_steps)
+    nvtx.range_pop()
     e2e_pipelined(3)
+    nvtx.range_push("e2e")
     ms_e2e = e2e_pipelined(e2e_steps)
+    nvtx.range_pop()
     clk = clocks.stop()
     status = G.coda_device_status(clear=True)
     h2d = sum(host[k].numel() * 2 for k in ("X", "W", "A", "B"))
