@@ -55,11 +55,13 @@ constexpr int kMaxInSlots = 4;
 // of 48 KiB. kCG = 4: a cluster of two SM pairs computes two 256 x 256 tiles
 // side by side in N; both pairs need the same A rows, so each CTA loads half
 // of its 128 A rows and multicasts them to its counterpart in the other pair
-// (a quarter less operand traffic from L2 per SM). kIn = input boxes per chunk (0, 1, 2), kInWarp = bytes of each
-// epilogue warp's input ring, kSlots = store boxes per staging buffer (1-3).
-// The mainloop gets as many stages as the shared memory left after the
-// epilogue's staging and input ring allows, at most 6 (pair) or 4 (single):
-// 6 / 4 without inputs, 5 / 3 with an 8 KiB ring or three staging boxes.
+// (a quarter less operand traffic from L2 per SM).
+// kIn = input boxes per chunk (0, 1, 2), kInWarp = bytes of each epilogue
+// warp's input ring, kSlots = store boxes per staging buffer (1-3), kBufs =
+// staging buffers, kShared = bytes of an epilogue-wide table. The mainloop gets
+// as many stages as the shared memory left after the epilogue's staging, input
+// ring and table allows, at most 6 (pair) or 4 (single): 6 / 4 without
+// inputs, 5 / 3 with an 8 KiB ring per warp or three staging boxes.
 template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes, int kBufs = kEpiBufs, int kShared = 0>
 struct Cfg {
   static constexpr int kPair = kCG == 1 ? 1 : 2;  // CTAs per MMA (cta_group)
