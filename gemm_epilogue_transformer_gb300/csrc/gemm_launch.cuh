@@ -10,7 +10,6 @@
 
 namespace coda {
 
-constexpr int kGroupM = 16;  // 128-row blocks per raster group
 // Two-box input epilogues keep two chunks of inputs in flight (a larger ring,
 // one mainloop stage less) when K is at most this: a mainloop that short
 // cannot hide one HBM round trip per chunk.
@@ -122,7 +121,17 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.n_blocks = (N + BN * C::kPairs - 1) / (BN * C::kPairs);  // column blocks of kPairs tiles
   p.k_blocks = kF8 ? (K + 2 * BK - 1) / (2 * BK) : (K + BK - 1) / BK;
   p.num_tiles = p.m_blocks * p.n_blocks;
-  p.group_m = p.m_blocks < kGroupM / C::kPair ? p.m_blocks : kGroupM / C::kPair;
+  // Raster group: the row blocks that sweep all column blocks together (tile
+  // order in tile_coords). B is read from DRAM once per group when it does not
+  // fit in L2, so a group of 4096 rows halves that traffic against 2048 rows;
+  // it is used when B exceeds half of L2 and the group's A rows (4096 x K)
+  // still fit in a third of it.
+  {
+    const double eb = kF8 ? 1.0 : 2.0, l2 = static_cast<double>(di->l2_bytes);
+    const bool wide = static_cast<double>(K) * N * eb > 0.5 * l2 && 4096.0 * K * eb <= l2 / 3.0;
+    const int gm = (wide ? 4096 : 2048) / C::kTileM;
+    p.group_m = p.m_blocks < gm ? p.m_blocks : gm;
+  }
   p.seg_blocks = (N + BSEG - 1) / BSEG;
   // Wave balance: a last wave of `rem` tiles that fills at most half of the
   // persistent clusters runs as 2 * rem half tiles (256 x 128 per pair) instead.

@@ -18,6 +18,7 @@ int fail_cuda(cudaError_t e, const char* what);
 struct DeviceInfo {
   int ok;
   int sm_count;
+  long long l2_bytes;  // L2 cache size
   int* status;  // device address of the status word
 };
 // Info for the current device (validated as sm_103); nullptr after fail().

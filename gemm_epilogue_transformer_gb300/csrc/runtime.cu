@@ -62,6 +62,7 @@ static const DeviceInfo* init_device(int dev) {
     return nullptr;
   }
   d.sm_count = prop.multiProcessorCount;
+  d.l2_bytes = prop.l2CacheSize;
   d.status = static_cast<int*>(p);
   d.ok = 1;
   return &d;
