@@ -3,6 +3,7 @@
 // values per tile instead of the full activation), plus the RoPE tables.
 // All are HBM/latency bound; one warp per row, coalesced over the partials.
 #include "host.h"
+#include "light_launch.cuh"
 
 using namespace coda;
 
@@ -27,6 +28,7 @@ __device__ __forceinline__ int warp_min_i(int v) {
 // r[i] = 1 / sqrt(sum_t psq[i,t] / d + eps)   (pith page, Figure 5 caption)
 __global__ void rms_reduce_kernel(int M, int nb, float inv_d, const float* __restrict__ psq, float eps,
                                   float* __restrict__ r) {
+  light_kernel_enter();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M; row += warps) {
@@ -40,6 +42,7 @@ __global__ void rms_reduce_kernel(int M, int nb, float inv_d, const float* __res
 // s[i] = sum_t pdot[i,t] / d   (CODA note, Key design 3)
 __global__ void rowdot_reduce_kernel(int M, int nb, float inv_d, const float* __restrict__ pdot,
                                      float* __restrict__ s_out) {
+  light_kernel_enter();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M; row += warps) {
@@ -56,6 +59,7 @@ __global__ void ce_reduce_kernel(int M, int nb, const float* __restrict__ pmax, 
                                  const int32_t* __restrict__ parg, const float* __restrict__ tgt,
                                  float* __restrict__ lse_out, float* __restrict__ loss_row,
                                  int32_t* __restrict__ argmax_out) {
+  light_kernel_enter();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < M; row += warps) {
@@ -84,6 +88,7 @@ __global__ void ce_reduce_kernel(int M, int nb, const float* __restrict__ pmax, 
 
 // Deterministic mean of loss_row in one block (double accumulation).
 __global__ void mean_kernel(int M, const float* __restrict__ v, float* __restrict__ out) {
+  light_kernel_enter();
   __shared__ double sh[32];
   double acc = 0.0;
   for (int i = threadIdx.x; i < M; i += blockDim.x) acc += static_cast<double>(v[i]);
@@ -106,6 +111,7 @@ __global__ void mean_kernel(int M, const float* __restrict__ v, float* __restric
 constexpr int kColsumWarps = 16;
 __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(int rows, int d, const float* __restrict__ pdg,
                                                                    float* __restrict__ out) {
+  light_kernel_enter();
   __shared__ float sh[kColsumWarps][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int j0 = blockIdx.x * 32; j0 < d; j0 += gridDim.x * 32) {
@@ -137,6 +143,7 @@ __global__ void __launch_bounds__(kColsumWarps * 32) colsum_kernel(int rows, int
 // cos/sin(p * theta^(-2i/head_dim)) in fp64, rounded to fp32.
 __global__ void rope_tables_kernel(int S, int half, int head_dim, double theta, float* __restrict__ c,
                                    float* __restrict__ s) {
+  light_kernel_enter();
   const long n = static_cast<long>(S) * half;
   for (long k = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; k < n;
        k += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -156,8 +163,7 @@ int row_grid(const DeviceInfo* di, int rows, int rows_per_block) {
   return static_cast<int>(g < cap ? (g > 0 ? g : 1) : cap);
 }
 
-int launched(const char* fn) {
-  cudaError_t e = cudaGetLastError();
+int launched(cudaError_t e, const char* fn) {
   return e == cudaSuccess ? CODA_OK : fail_cuda(e, fn);
 }
 
@@ -175,8 +181,8 @@ int coda_rms_reduce(int M, int nb, int d, const float* psq, float eps, float* r_
   CODA_REQ_PTR4(r_out);
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
-  rms_reduce_kernel<<<row_grid(di, M, 8), 256, 0, as_stream(stream)>>>(M, nb, 1.0f / d, psq, eps, r_out);
-  return launched(fn);
+  return launched(launch_light(rms_reduce_kernel, row_grid(di, M, 8), 256, 0, as_stream(stream), M, nb, 1.0f / d, psq,
+                               eps, r_out), fn);
 }
 
 int coda_rowdot_reduce(int M, int nb, int d, const float* pdot, float* s_out, coda_stream_t stream) {
@@ -188,8 +194,8 @@ int coda_rowdot_reduce(int M, int nb, int d, const float* pdot, float* s_out, co
   CODA_REQ_PTR4(s_out);
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
-  rowdot_reduce_kernel<<<row_grid(di, M, 8), 256, 0, as_stream(stream)>>>(M, nb, 1.0f / d, pdot, s_out);
-  return launched(fn);
+  return launched(launch_light(rowdot_reduce_kernel, row_grid(di, M, 8), 256, 0, as_stream(stream), M, nb, 1.0f / d,
+                               pdot, s_out), fn);
 }
 
 int coda_ce_reduce(int M, int nb, const float* pmax, const float* psum, const int32_t* parg, const float* tgt,
@@ -210,12 +216,10 @@ int coda_ce_reduce(int M, int nb, const float* pmax, const float* psum, const in
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
-  ce_reduce_kernel<<<row_grid(di, M, 8), 256, 0, st>>>(M, nb, pmax, psum, parg, tgt, lse_out, loss_row_out,
-                                                       argmax_out);
-  int rc = launched(fn);
+  int rc = launched(launch_light(ce_reduce_kernel, row_grid(di, M, 8), 256, 0, st, M, nb, pmax, psum, parg, tgt,
+                                 lse_out, loss_row_out, argmax_out), fn);
   if (rc || !loss_mean_out) return rc;
-  mean_kernel<<<1, 1024, 0, st>>>(M, loss_row_out, loss_mean_out);
-  return launched(fn);
+  return launched(launch_light(mean_kernel, 1, 1024, 0, st, M, loss_row_out, loss_mean_out), fn);
 }
 
 int coda_colsum_reduce(int rows, int d, const float* pdg, float* dgamma_out, coda_stream_t stream) {
@@ -228,8 +232,8 @@ int coda_colsum_reduce(int rows, int d, const float* pdg, float* dgamma_out, cod
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int strips = (d + 31) / 32;
   const int grid = strips < di->sm_count * 4 ? strips : di->sm_count * 4;
-  colsum_kernel<<<grid, kColsumWarps * 32, 0, as_stream(stream)>>>(rows, d, pdg, dgamma_out);
-  return launched(fn);
+  return launched(launch_light(colsum_kernel, grid, kColsumWarps * 32, 0, as_stream(stream), rows, d, pdg, dgamma_out),
+                  fn);
 }
 
 int coda_rope_tables(int S, int head_dim, double theta, float* cos_out, float* sin_out, coda_stream_t stream) {
@@ -243,9 +247,8 @@ int coda_rope_tables(int S, int head_dim, double theta, float* cos_out, float* s
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int half = head_dim / 2;
-  rope_tables_kernel<<<row_grid(di, S * half, 256), 256, 0, as_stream(stream)>>>(S, half, head_dim, theta, cos_out,
-                                                                                  sin_out);
-  return launched(fn);
+  return launched(launch_light(rope_tables_kernel, row_grid(di, S * half, 256), 256, 0, as_stream(stream), S, half,
+                               head_dim, theta, cos_out, sin_out), fn);
 }
 
 }  // extern "C"
