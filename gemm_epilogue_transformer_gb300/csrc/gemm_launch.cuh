@@ -5,6 +5,8 @@
 
 #include <string.h>
 
+#include <atomic>
+
 #include "epilogues.cuh"
 #include "host.h"
 
@@ -80,7 +82,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
     if (rc) return rc;
   }
   auto kernel = &gemm_epilogue_kernel<Epi, kCG, kF8>;
-  static int max_clusters[64] = {0};  // per device; 0 = not yet queried
+  static std::atomic<int> max_clusters[64] = {};  // per device; 0 = not yet queried (any thread may fill it)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return fail(CODA_ERR_INVALID, "%s: device index %d", fn, dev);

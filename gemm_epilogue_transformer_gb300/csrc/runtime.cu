@@ -13,8 +13,9 @@
 namespace coda {
 
 static thread_local char g_err[1024] = "";
-static unsigned long long g_timeout_ns = 2000000000ull;
-static int g_cta_group = 0;
+// settings written by coda_set_* and read at every launch, possibly from other host threads
+static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+static std::atomic<int> g_cta_group{0};
 static std::atomic<int> g_inject{0};
 
 // The device status word (CODA_DEVST_* bits). Kernels receive its device
