@@ -1,8 +1,9 @@
 """Outputs past 2^31 elements.
 
-The plain GEMM and the fused RoPE GEMM write a [65568, 33024] bf16 output
-(2.17e9 elements, 4.3 GB), ragged in both dimensions (M is 32 rows past a
-256-row tile, N 256 columns past a 512-column block). Sampled rows, among them
+The plain GEMM, the unfused in-place RoPE and the fused RoPE GEMM write a
+[65568, 33024] bf16 output (2.17e9 elements, 4.3 GB), ragged in both
+dimensions (M is 32 rows past a 256-row tile, N 256 columns past a 512-column
+block). Sampled rows, among them
 rows whose flat offsets lie past 2^31, are checked against the float64 oracle
 (positions = row mod S for RoPE, so the tables wrap 16 times). This guards
 every offset on the path (TMA coordinates, tile and item counters, the
@@ -32,9 +33,14 @@ def test_output_past_2_31_elements(coda):
     out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
 
     coda.coda_gemm(X, W, out=out)
-    assert_bf16(f64(out[rows]), O.matmul(X64, W64), "plain GEMM rows")
+    plain = f64(out[rows])
+    assert_bf16(plain, O.matmul(X64, W64), "plain GEMM rows")
 
+    # the unfused comparison path's in-place rotation over the same buffer
     c, s = coda.coda_rope_tables(S, hd, 10000.0)
+    coda.coda_unfused_rope(out, c, s, hd, rc)
+    assert_bf16(f64(out[rows]), O.rope(plain, rows % S, hd, 10000.0, rc), "unfused RoPE rows")
+
     out.fill_(float("nan"))
     coda.coda_gemm_rope(X, W, c, s, hd, rc, out=out)
     assert_bf16(f64(out[rows]), O.gemm_rope(X64, W64, rows % S, hd, 10000.0, rc), "RoPE GEMM rows")
