@@ -24,6 +24,13 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and do not synchronise. Outputs must not alias inputs
  *     unless stated.
+ *   - The fused GEMMs and the auxiliary reductions are launched with
+ *     programmatic stream serialization: each kernel may be scheduled while
+ *     the previous kernel on the stream finishes, and waits for it
+ *     (griddepcontrol.wait) before touching memory, so stream order holds as
+ *     for plain launches. A caller's own kernel launched after a coda call
+ *     with the same attribute must likewise wait (cudaGridDependencySynchronize)
+ *     before reading the call's outputs.
  *   - A dimension of 0 makes the call a no-op that returns CODA_OK (an empty
  *     contraction, K = 0, gives a zero accumulator and the epilogue still runs).
  *   - Return value: CODA_OK, or a negative CODA_ERR_*; coda_last_error()
