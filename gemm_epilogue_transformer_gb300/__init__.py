@@ -54,30 +54,64 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _bf16(t, name, ndim=None):
-    if t.dtype != torch.bfloat16 or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA bfloat16 tensor (got {t.dtype} on {t.device})")
+def _on_device(t, name):
+    """The kernels run on the current CUDA device and read every pointer there."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (got {type(t).__name__}"
+                        f"{' on ' + str(t.device) if isinstance(t, torch.Tensor) else ''})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()}")
+    return t
+
+
+def _typed(t, name, dtype, ndim=None, shape=None):
+    """Dtype, device, contiguity and (optionally) rank and exact shape of a tensor
+    the kernels read or write: a mismatch here would become an out-of-bounds
+    access on the device, so it is rejected before the call."""
+    _on_device(t, name)
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims (got {tuple(t.shape)})")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
 
 
-def _f32(t, name):
-    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
-    return t
+def _bf16(t, name, ndim=None, shape=None):
+    return _typed(t, name, torch.bfloat16, ndim, shape)
 
 
-def _i32(t, name):
-    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
-    return t
+def _f32(t, name, shape=None):
+    return _typed(t, name, torch.float32, None, shape)
+
+
+def _i32(t, name, shape=None):
+    return _typed(t, name, torch.int32, None, shape)
 
 
 def _empty(shape, dtype, like):
     return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def _out(t, shape, dtype, like, name="out"):
+    """A caller-provided output buffer, checked like an input; else a new one."""
+    return _empty(shape, dtype, like) if t is None else _typed(t, name, dtype, None, shape)
+
+
+def _mismatch(args) -> str:
+    """Message for inconsistent operand shapes, listing every tensor argument."""
+    shapes = ", ".join(f"{k} {tuple(v.shape)}" for k, v in args.items() if isinstance(v, torch.Tensor))
+    return f"shape mismatch: {shapes}"
+
+
+def _tables(cos, sin, head_dim):
+    _f32(cos, "cos", None), _f32(sin, "sin", None)
+    if cos.dim() != 2 or cos.shape != sin.shape or cos.shape[1] != head_dim // 2:
+        raise ValueError(f"cos and sin must both be [S, head_dim/2 = {head_dim // 2}] "
+                         f"(got {tuple(cos.shape)} and {tuple(sin.shape)})")
 
 
 # ----------------------------------------------------------------- runtime
@@ -120,8 +154,10 @@ def coda_num_row_tiles(M: int) -> int:
 
 def coda_gemm(A, B, transA: bool = False, transB: bool = False, out=None, stream=None):
     """C = op(A) op(B). A is [M,K] (or [K,M] with transA), B is [K,N] (or [N,K])."""
-    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
-        raise TypeError("A and B must be bfloat16")
+    for t, nm in ((A, "A"), (B, "B")):
+        _on_device(t, nm)
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{nm} must be bfloat16 (got {t.dtype})")
     if A.dim() != 2 or B.dim() != 2 or A.stride(1) != 1 or B.stride(1) != 1:
         raise ValueError("A and B must be 2-D with unit column stride")
     M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
@@ -130,8 +166,9 @@ def coda_gemm(A, B, transA: bool = False, transB: bool = False, out=None, stream
         raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
     if out is None:
         out = _empty((M, N), torch.bfloat16, A)
-    if out.stride(1) != 1:
-        raise ValueError("out must have unit column stride")
+    _on_device(out, "out")
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError(f"out must be a bfloat16 [{M}, {N}] tensor with unit column stride")
     _check(lib().coda_gemm(M, N, K, _ptr(A), A.stride(0), int(transA), _ptr(B), B.stride(0), int(transB),
                            _ptr(out), out.stride(0), _stream(stream)))
     return out
@@ -143,10 +180,10 @@ def coda_gemm_res_rmsprep(x, W0, z, gamma, h1=None, h2=None, psq=None, stream=No
     M, K = x.shape
     N = W0.shape[1]
     if W0.shape[0] != K or z.shape != (M, N) or gamma.shape[0] != N:
-        raise ValueError("shape mismatch")
-    h1 = _empty((M, N), torch.bfloat16, x) if h1 is None else h1
-    h2 = _empty((M, N), torch.bfloat16, x) if h2 is None else h2
-    psq = _empty((M, coda_num_col_tiles(N)), torch.float32, x) if psq is None else psq
+        raise ValueError(_mismatch(locals()))
+    h1 = _out(h1, (M, N), torch.bfloat16, x, "h1")
+    h2 = _out(h2, (M, N), torch.bfloat16, x, "h2")
+    psq = _out(psq, (M, coda_num_col_tiles(N)), torch.float32, x, "psq")
     _check(lib().coda_gemm_res_rmsprep(M, N, K, _ptr(x), _ptr(W0), _ptr(z), _ptr(gamma), _ptr(h1), _ptr(h2),
                                        _ptr(psq), _stream(stream)))
     return h1, h2, psq
@@ -154,8 +191,10 @@ def coda_gemm_res_rmsprep(x, W0, z, gamma, h1=None, h2=None, psq=None, stream=No
 
 def coda_rms_reduce(psq, d: int, eps: float, r=None, stream=None):
     _f32(psq, "psq")
+    if psq.dim() != 2:
+        raise ValueError("psq must be [M, nb]")
     M, nb = psq.shape
-    r = _empty((M,), torch.float32, psq) if r is None else r
+    r = _out(r, (M,), torch.float32, psq, "r")
     _check(lib().coda_rms_reduce(M, nb, d, _ptr(psq), float(eps), _ptr(r), _stream(stream)))
     return r
 
@@ -165,8 +204,8 @@ def coda_gemm_rowscale(h2, W1, r, out=None, stream=None):
     M, K = h2.shape
     N = W1.shape[1]
     if W1.shape[0] != K or r.shape[0] != M:
-        raise ValueError("shape mismatch")
-    out = _empty((M, N), torch.bfloat16, h2) if out is None else out
+        raise ValueError(_mismatch(locals()))
+    out = _out(out, (M, N), torch.bfloat16, h2)
     _check(lib().coda_gemm_rowscale(M, N, K, _ptr(h2), _ptr(W1), _ptr(r), _ptr(out), _stream(stream)))
     return out
 
@@ -177,23 +216,23 @@ def coda_gemm_swiglu(X, Wgu, want_gu: bool = False, out=None, gu=None, stream=No
     M, K = X.shape
     F2 = Wgu.shape[1]
     if Wgu.shape[0] != K or F2 % 2:
-        raise ValueError("shape mismatch")
+        raise ValueError(_mismatch(locals()))
     F = F2 // 2
-    out = _empty((M, F), torch.bfloat16, X) if out is None else out
-    if want_gu and gu is None:
-        gu = _empty((M, F2), torch.bfloat16, X)
+    out = _out(out, (M, F), torch.bfloat16, X)
+    gu = _out(gu, (M, F2), torch.bfloat16, X, "gu") if (want_gu or gu is not None) else None
     _check(lib().coda_gemm_swiglu(M, F, K, _ptr(X), _ptr(Wgu), _ptr(out), _ptr(gu), _stream(stream)))
     return out, gu
 
 
 def coda_gemm_swiglu_bwd(dY, Wd, gu, out=None, stream=None):
     """dGU (interleaved dG, dU) from dA = dY Wd^T; Wd stored [F, K]."""
-    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2), _bf16(gu, "gu", 2)
+    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2)
     M, K = dY.shape
     F = Wd.shape[0]
-    if Wd.shape[1] != K or gu.shape != (M, 2 * F):
-        raise ValueError("shape mismatch")
-    out = _empty((M, 2 * F), torch.bfloat16, dY) if out is None else out
+    if Wd.shape[1] != K:
+        raise ValueError(f"Wd must be [F, K = {K}] (got {tuple(Wd.shape)})")
+    _bf16(gu, "gu", 2, (M, 2 * F))
+    out = _out(out, (M, 2 * F), torch.bfloat16, dY)
     _check(lib().coda_gemm_swiglu_bwd(M, F, K, _ptr(dY), _ptr(Wd), _ptr(gu), _ptr(out), _stream(stream)))
     return out
 
@@ -207,12 +246,12 @@ def coda_rope_tables(S: int, head_dim: int, theta: float, device=None, stream=No
 
 
 def _rope(fname, X, W, cos, sin, head_dim, rope_cols, out, stream):
-    _bf16(X, "X", 2), _bf16(W, "W", 2), _f32(cos, "cos"), _f32(sin, "sin")
+    _bf16(X, "X", 2), _bf16(W, "W", 2), _tables(cos, sin, head_dim)
     M, K = X.shape
     N = W.shape[1]
-    if W.shape[0] != K or cos.shape != sin.shape or cos.shape[1] != head_dim // 2:
-        raise ValueError("shape mismatch")
-    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    if W.shape[0] != K:
+        raise ValueError(_mismatch(locals()))
+    out = _out(out, (M, N), torch.bfloat16, X)
     _check(getattr(lib(), fname)(M, N, K, _ptr(X), _ptr(W), _ptr(cos), _ptr(sin), cos.shape[0], head_dim,
                                  rope_cols, _ptr(out), _stream(stream)))
     return out
@@ -233,7 +272,7 @@ def coda_gemm_ce_lse(H, W, labels, with_argmax: bool = True, stream=None):
     M, K = H.shape
     V = W.shape[1]
     if W.shape[0] != K or labels.shape[0] != M:
-        raise ValueError("shape mismatch")
+        raise ValueError(_mismatch(locals()))
     nb = coda_num_col_tiles(V)
     pmax = _empty((M, nb), torch.float32, H)
     psum = _empty((M, nb), torch.float32, H)
@@ -246,7 +285,13 @@ def coda_gemm_ce_lse(H, W, labels, with_argmax: bool = True, stream=None):
 
 def coda_ce_reduce(pmax, psum, parg, tgt, stream=None):
     """Returns (lse, loss_row, loss_mean[1], argmax or None)."""
+    _f32(pmax, "pmax")
+    if pmax.dim() != 2:
+        raise ValueError("pmax must be [M, nb]")
     M, nb = pmax.shape
+    _f32(psum, "psum", (M, nb)), _f32(tgt, "tgt", (M,))
+    if parg is not None:
+        _i32(parg, "parg", (M, nb))
     lse = _empty((M,), torch.float32, pmax)
     loss_row = _empty((M,), torch.float32, pmax)
     loss_mean = _empty((1,), torch.float32, pmax)
@@ -257,10 +302,13 @@ def coda_ce_reduce(pmax, psum, parg, tgt, stream=None):
 
 
 def coda_gemm_ce_bwd(H, W, labels, lse, grad_scale: float, out=None, stream=None):
-    _bf16(H, "H", 2), _bf16(W, "W", 2), _i32(labels, "labels"), _f32(lse, "lse")
+    _bf16(H, "H", 2), _bf16(W, "W", 2)
     M, K = H.shape
     V = W.shape[1]
-    out = _empty((M, V), torch.bfloat16, H) if out is None else out
+    if W.shape[0] != K:
+        raise ValueError(_mismatch(locals()))
+    _i32(labels, "labels", (M,)), _f32(lse, "lse", (M,))
+    out = _out(out, (M, V), torch.bfloat16, H)
     _check(lib().coda_gemm_ce_bwd(M, V, K, _ptr(H), _ptr(W), _ptr(labels), _ptr(lse), float(grad_scale),
                                   _ptr(out), _stream(stream)))
     return out
@@ -268,9 +316,16 @@ def coda_gemm_ce_bwd(H, W, labels, lse, grad_scale: float, out=None, stream=None
 
 def coda_gemm_rowdot(dO, Wn, Y, r=None, want_dyr: bool = True, stream=None):
     """dY = dO Wn, dYr = r * dY (optional), pdot tile partials of rowsum(dY * Y)."""
-    _bf16(dO, "dO", 2), _bf16(Wn, "Wn", 2), _bf16(Y, "Y", 2)
+    _bf16(dO, "dO", 2), _bf16(Wn, "Wn", 2)
     M, K = dO.shape
     N = Wn.shape[1]
+    if Wn.shape[0] != K:
+        raise ValueError(_mismatch(locals()))
+    _bf16(Y, "Y", 2, (M, N))
+    if want_dyr:
+        if r is None:
+            raise ValueError("r is required for the dYr side output")
+        _f32(r, "r", (M,))
     dY = _empty((M, N), torch.bfloat16, dO)
     dYr = _empty((M, N), torch.bfloat16, dO) if want_dyr else None
     pdot = _empty((M, coda_num_col_tiles(N)), torch.float32, dO)
@@ -280,6 +335,9 @@ def coda_gemm_rowdot(dO, Wn, Y, r=None, want_dyr: bool = True, stream=None):
 
 
 def coda_rowdot_reduce(pdot, d: int, stream=None):
+    _f32(pdot, "pdot")
+    if pdot.dim() != 2:
+        raise ValueError("pdot must be [M, nb]")
     M, nb = pdot.shape
     s = _empty((M,), torch.float32, pdot)
     _check(lib().coda_rowdot_reduce(M, nb, d, _ptr(pdot), _ptr(s), _stream(stream)))
@@ -288,10 +346,12 @@ def coda_rowdot_reduce(pdot, d: int, stream=None):
 
 def coda_gemm_rmsnorm_bwd(dY, W1, h1, gamma, r, s, stream=None):
     """dh1 = r gamma G - r^2 s h1 with G = dY W1^T (W1 stored [d, K]); pdg column partials."""
-    _bf16(dY, "dY", 2), _bf16(W1, "W1", 2), _bf16(h1, "h1", 2), _bf16(gamma, "gamma", 1)
-    _f32(r, "r"), _f32(s, "s")
+    _bf16(dY, "dY", 2), _bf16(W1, "W1", 2)
     M, K = dY.shape
     d = W1.shape[0]
+    if W1.shape[1] != K:
+        raise ValueError(_mismatch(locals()))
+    _bf16(h1, "h1", 2, (M, d)), _bf16(gamma, "gamma", 1, (d,)), _f32(r, "r", (M,)), _f32(s, "s", (M,))
     dh1 = _empty((M, d), torch.bfloat16, dY)
     pdg = _empty((coda_num_row_tiles(M), d), torch.float32, dY)
     _check(lib().coda_gemm_rmsnorm_bwd(M, d, K, _ptr(dY), _ptr(W1), _ptr(h1), _ptr(gamma), _ptr(r), _ptr(s),
@@ -300,6 +360,9 @@ def coda_gemm_rmsnorm_bwd(dY, W1, h1, gamma, r, s, stream=None):
 
 
 def coda_colsum_reduce(pdg, stream=None):
+    _f32(pdg, "pdg")
+    if pdg.dim() != 2:
+        raise ValueError("pdg must be [rows, d]")
     rows, d = pdg.shape
     out = _empty((d,), torch.float32, pdg)
     _check(lib().coda_colsum_reduce(rows, d, _ptr(pdg), _ptr(out), _stream(stream)))
@@ -309,14 +372,18 @@ def coda_colsum_reduce(pdg, stream=None):
 # ----------------------------------------------------------------- unfused path
 
 def coda_unfused_add(a, b, out=None, stream=None):
+    _bf16(a, "a", 2)
     M, N = a.shape
-    out = torch.empty_like(a) if out is None else out
+    _bf16(b, "b", 2, (M, N))
+    out = _out(out, (M, N), torch.bfloat16, a)
     _check(lib().coda_unfused_add(M, N, _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
     return out
 
 
 def coda_unfused_rmsnorm(h, gamma, eps: float, stream=None):
+    _bf16(h, "h", 2)
     M, d = h.shape
+    _bf16(gamma, "gamma", 1, (d,))
     n = torch.empty_like(h)
     r = _empty((M,), torch.float32, h)
     _check(lib().coda_unfused_rmsnorm(M, d, _ptr(h), _ptr(gamma), float(eps), _ptr(n), _ptr(r), _stream(stream)))
@@ -324,21 +391,28 @@ def coda_unfused_rmsnorm(h, gamma, eps: float, stream=None):
 
 
 def coda_unfused_rowscale(x, r, stream=None):
+    _bf16(x, "x", 2)
     M, N = x.shape
+    _f32(r, "r", (M,))
     out = torch.empty_like(x)
     _check(lib().coda_unfused_rowscale(M, N, _ptr(x), _ptr(r), _ptr(out), _stream(stream)))
     return out
 
 
 def coda_unfused_swiglu(gu, stream=None):
+    _bf16(gu, "gu", 2)
     M, F2 = gu.shape
+    if F2 % 2:
+        raise ValueError("gu must have an even number of columns (gate/up pairs)")
     out = _empty((M, F2 // 2), torch.bfloat16, gu)
     _check(lib().coda_unfused_swiglu(M, F2 // 2, _ptr(gu), _ptr(out), _stream(stream)))
     return out
 
 
 def coda_unfused_swiglu_bwd(dA, gu, stream=None):
+    _bf16(dA, "dA", 2)
     M, F = dA.shape
+    _bf16(gu, "gu", 2, (M, 2 * F))
     out = _empty((M, 2 * F), torch.bfloat16, dA)
     _check(lib().coda_unfused_swiglu_bwd(M, F, _ptr(dA), _ptr(gu), _ptr(out), _stream(stream)))
     return out
@@ -346,6 +420,7 @@ def coda_unfused_swiglu_bwd(dA, gu, stream=None):
 
 def coda_unfused_rope(x, cos, sin, head_dim: int, rope_cols: int, stream=None):
     """In place on x [M, N]."""
+    _bf16(x, "x", 2), _tables(cos, sin, head_dim)
     M, N = x.shape
     _check(lib().coda_unfused_rope(M, N, _ptr(cos), _ptr(sin), cos.shape[0], head_dim, rope_cols, _ptr(x),
                                    _stream(stream)))
@@ -353,6 +428,7 @@ def coda_unfused_rope(x, cos, sin, head_dim: int, rope_cols: int, stream=None):
 
 
 def coda_unfused_rope_bwd(x, cos, sin, head_dim: int, rope_cols: int, stream=None):
+    _bf16(x, "x", 2), _tables(cos, sin, head_dim)
     M, N = x.shape
     _check(lib().coda_unfused_rope_bwd(M, N, _ptr(cos), _ptr(sin), cos.shape[0], head_dim, rope_cols, _ptr(x),
                                        _stream(stream)))
@@ -360,7 +436,9 @@ def coda_unfused_rope_bwd(x, cos, sin, head_dim: int, rope_cols: int, stream=Non
 
 
 def coda_unfused_ce_fwd(logits, labels, stream=None):
+    _bf16(logits, "logits", 2)
     M, V = logits.shape
+    _i32(labels, "labels", (M,))
     lse = _empty((M,), torch.float32, logits)
     loss_row = _empty((M,), torch.float32, logits)
     loss_mean = _empty((1,), torch.float32, logits)
@@ -371,7 +449,9 @@ def coda_unfused_ce_fwd(logits, labels, stream=None):
 
 
 def coda_unfused_ce_bwd(logits, labels, lse, grad_scale: float, stream=None):
+    _bf16(logits, "logits", 2)
     M, V = logits.shape
+    _i32(labels, "labels", (M,)), _f32(lse, "lse", (M,))
     out = torch.empty_like(logits)
     _check(lib().coda_unfused_ce_bwd(M, V, _ptr(logits), _ptr(labels), _ptr(lse), float(grad_scale), _ptr(out),
                                      _stream(stream)))
@@ -379,14 +459,18 @@ def coda_unfused_ce_bwd(logits, labels, lse, grad_scale: float, stream=None):
 
 
 def coda_unfused_rowdot(dY, Y, d: int, stream=None):
+    _bf16(dY, "dY", 2)
     M, N = dY.shape
+    _bf16(Y, "Y", 2, (M, N))
     s = _empty((M,), torch.float32, dY)
     _check(lib().coda_unfused_rowdot(M, N, d, _ptr(dY), _ptr(Y), _ptr(s), _stream(stream)))
     return s
 
 
 def coda_unfused_rmsnorm_bwd(G, h, gamma, r, stream=None):
+    _bf16(G, "G", 2)
     M, d = G.shape
+    _bf16(h, "h", 2, (M, d)), _bf16(gamma, "gamma", 1, (d,)), _f32(r, "r", (M,))
     dh = torch.empty_like(G)
     pdg = _empty((coda_num_row_tiles(M), d), torch.float32, G)
     _check(lib().coda_unfused_rmsnorm_bwd(M, d, _ptr(G), _ptr(h), _ptr(gamma), _ptr(r), _ptr(dh), _ptr(pdg),
@@ -398,12 +482,13 @@ def coda_unfused_rmsnorm_bwd(G, h, gamma, r, stream=None):
 
 def coda_gemm_rowscale_rope(X, W, r, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
     """out = RoPE(r * (X W)) (row scale and rotation in one epilogue)."""
-    _bf16(X, "X", 2), _bf16(W, "W", 2), _f32(r, "r"), _f32(cos, "cos"), _f32(sin, "sin")
+    _bf16(X, "X", 2), _bf16(W, "W", 2), _tables(cos, sin, head_dim)
     M, K = X.shape
     N = W.shape[1]
-    if W.shape[0] != K or r.shape[0] != M or cos.shape != sin.shape or cos.shape[1] != head_dim // 2:
-        raise ValueError("shape mismatch")
-    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    if W.shape[0] != K:
+        raise ValueError(_mismatch(locals()))
+    _f32(r, "r", (M,))
+    out = _out(out, (M, N), torch.bfloat16, X)
     _check(lib().coda_gemm_rowscale_rope(M, N, K, _ptr(X), _ptr(W), _ptr(r), _ptr(cos), _ptr(sin), cos.shape[0],
                                          head_dim, rope_cols, _ptr(out), _stream(stream)))
     return out
@@ -411,15 +496,15 @@ def coda_gemm_rowscale_rope(X, W, r, cos, sin, head_dim: int, rope_cols: int, ou
 
 def coda_gemm_rowscale_swiglu(X, Wgu, r, want_gu: bool = False, out=None, gu=None, stream=None):
     """GU = r * (X Wgu), A = silu(G) * U; returns (A, GU or None)."""
-    _bf16(X, "X", 2), _bf16(Wgu, "Wgu", 2), _f32(r, "r")
+    _bf16(X, "X", 2), _bf16(Wgu, "Wgu", 2)
     M, K = X.shape
     F2 = Wgu.shape[1]
-    if Wgu.shape[0] != K or F2 % 2 or r.shape[0] != M:
-        raise ValueError("shape mismatch")
+    if Wgu.shape[0] != K or F2 % 2:
+        raise ValueError(_mismatch(locals()))
+    _f32(r, "r", (M,))
     F = F2 // 2
-    out = _empty((M, F), torch.bfloat16, X) if out is None else out
-    if want_gu and gu is None:
-        gu = _empty((M, F2), torch.bfloat16, X)
+    out = _out(out, (M, F), torch.bfloat16, X)
+    gu = _out(gu, (M, F2), torch.bfloat16, X, "gu") if (want_gu or gu is not None) else None
     _check(lib().coda_gemm_rowscale_swiglu(M, F, K, _ptr(X), _ptr(Wgu), _ptr(r), _ptr(out), _ptr(gu),
                                            _stream(stream)))
     return out, gu
@@ -428,11 +513,12 @@ def coda_gemm_rowscale_swiglu(X, Wgu, r, want_gu: bool = False, out=None, gu=Non
 def coda_gemm_swiglu_bwd_rowdot(dY, Wd, gu, r, stream=None):
     """dGUr = r * SwiGLU'(dY Wd^T; gu) and the row-statistic partials of dGU * gu.
     Returns (dgur [M,2F], pdot [M, ceil(F/128)])."""
-    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2), _bf16(gu, "gu", 2), _f32(r, "r")
+    _bf16(dY, "dY", 2), _bf16(Wd, "Wd", 2)
     M, K = dY.shape
     F = Wd.shape[0]
-    if Wd.shape[1] != K or gu.shape != (M, 2 * F) or r.shape[0] != M:
-        raise ValueError("shape mismatch")
+    if Wd.shape[1] != K:
+        raise ValueError(_mismatch(locals()))
+    _bf16(gu, "gu", 2, (M, 2 * F)), _f32(r, "r", (M,))
     dgur = _empty((M, 2 * F), torch.bfloat16, dY)
     pdot = _empty((M, coda_num_col_tiles(F)), torch.float32, dY)
     _check(lib().coda_gemm_swiglu_bwd_rowdot(M, F, K, _ptr(dY), _ptr(Wd), _ptr(gu), _ptr(r), _ptr(dgur), _ptr(pdot),
@@ -442,12 +528,13 @@ def coda_gemm_swiglu_bwd_rowdot(dY, Wd, gu, r, stream=None):
 
 def coda_gemm_rmsnorm_bwd_res(dYr, W1, h, gamma, r, s, dres, stream=None):
     """dh = gamma * (dYr W1^T) - r^2 s h + dres (W1 stored [d, K]); returns (dh, pdg)."""
-    _bf16(dYr, "dYr", 2), _bf16(W1, "W1", 2), _bf16(h, "h", 2), _bf16(gamma, "gamma", 1), _bf16(dres, "dres", 2)
-    _f32(r, "r"), _f32(s, "s")
+    _bf16(dYr, "dYr", 2), _bf16(W1, "W1", 2)
     M, K = dYr.shape
     d = W1.shape[0]
-    if W1.shape[1] != K or h.shape != (M, d) or dres.shape != (M, d):
-        raise ValueError("shape mismatch")
+    if W1.shape[1] != K:
+        raise ValueError(_mismatch(locals()))
+    _bf16(h, "h", 2, (M, d)), _bf16(gamma, "gamma", 1, (d,)), _bf16(dres, "dres", 2, (M, d))
+    _f32(r, "r", (M,)), _f32(s, "s", (M,))
     dh = _empty((M, d), torch.bfloat16, dYr)
     pdg = _empty((coda_num_row_tiles(M), d), torch.float32, dYr)
     _check(lib().coda_gemm_rmsnorm_bwd_res(M, d, K, _ptr(dYr), _ptr(W1), _ptr(h), _ptr(gamma), _ptr(r), _ptr(s),
@@ -457,10 +544,9 @@ def coda_gemm_rmsnorm_bwd_res(dYr, W1, h, gamma, r, s, dres, stream=None):
 
 def coda_rope_bwd_rowdot(dqkv, qkv, r, cos, sin, head_dim: int, rope_cols: int, d: int, stream=None):
     """dqr = r * RoPE^T(dqkv), s = (1/d) rowsum(dqkv * qkv); returns (dqr, s)."""
-    _bf16(dqkv, "dqkv", 2), _bf16(qkv, "qkv", 2), _f32(r, "r"), _f32(cos, "cos"), _f32(sin, "sin")
+    _bf16(dqkv, "dqkv", 2), _tables(cos, sin, head_dim)
     M, N = dqkv.shape
-    if qkv.shape != (M, N) or r.shape[0] != M:
-        raise ValueError("shape mismatch")
+    _bf16(qkv, "qkv", 2, (M, N)), _f32(r, "r", (M,))
     dqr = torch.empty_like(dqkv)
     s = _empty((M,), torch.float32, dqkv)
     _check(lib().coda_rope_bwd_rowdot(M, N, _ptr(dqkv), _ptr(qkv), _ptr(r), _ptr(cos), _ptr(sin), cos.shape[0],
@@ -486,11 +572,14 @@ class CodaBlock:
     _IN = ("P", "x", "O", "Wd", "gamma1", "Wqkv", "Wo", "gamma2", "Wgu")
 
     def __init__(self, t: dict, head_dim: int, rope_cols: int, cos, sin, eps: float = 1e-6, unfused: bool = False):
-        for k in self._IN:
-            _bf16(t[k], k)
-        _f32(cos, "cos"), _f32(sin, "sin")
+        _bf16(t["P"], "P", 2), _bf16(t["x"], "x", 2)
         M, F = t["P"].shape
         d = t["x"].shape[1]
+        shapes = {"P": (M, F), "x": (M, d), "O": (M, d), "Wd": (F, d), "gamma1": (d,), "Wqkv": (d, 3 * d),
+                  "Wo": (d, d), "gamma2": (d,), "Wgu": (d, 2 * F), "dQKV": (M, 3 * d), "gh": (M, d), "Wdn": (F, d)}
+        for k in self._IN:
+            _bf16(t[k], k, None, shapes[k])
+        _tables(cos, sin, head_dim)
         dev = t["x"]
         bf, f32 = torch.bfloat16, torch.float32
         self.M, self.d, self.F = M, d, F
@@ -518,7 +607,7 @@ class CodaBlock:
             setattr(b, k, _ptr(getattr(self, k)))
         for k, f in (("dQKV", "dqkv"), ("gh", "gh"), ("Wdn", "Wdn")):
             if k in t:
-                _bf16(t[k], k)
+                _bf16(t[k], k, None, shapes[k])
                 setattr(b, f, _ptr(t[k]))
         b.workspace = ws
         self._b = b
@@ -553,7 +642,8 @@ def _e4m3(t, name):
         if str(t.dtype) != "torch.float8_e4m3fn":
             raise TypeError(f"{name} must be a CUDA uint8 or float8_e4m3fn tensor (got {t.dtype})")
         t = t.view(torch.uint8)
-    if not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+    _on_device(t, name)
+    if not t.is_contiguous() or t.dim() != 2:
         raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
     return t
 
@@ -564,20 +654,20 @@ def coda_gemm_fp8(A, B, alpha: float, out=None, stream=None):
     M, K = A.shape
     N = B.shape[0]
     if B.shape[1] != K:
-        raise ValueError("shape mismatch")
-    out = _empty((M, N), torch.bfloat16, A) if out is None else out
+        raise ValueError(_mismatch(locals()))
+    out = _out(out, (M, N), torch.bfloat16, A)
     _check(lib().coda_gemm_fp8(M, N, K, _ptr(A), _ptr(B), float(alpha), _ptr(out), _stream(stream)))
     return out
 
 
 def coda_gemm_rope_fp8(X, W, alpha: float, cos, sin, head_dim: int, rope_cols: int, out=None, stream=None):
     X, W = _e4m3(X, "X"), _e4m3(W, "W")
-    _f32(cos, "cos"), _f32(sin, "sin")
+    _tables(cos, sin, head_dim)
     M, K = X.shape
     N = W.shape[0]
-    if W.shape[1] != K or cos.shape[1] != head_dim // 2:
-        raise ValueError("shape mismatch")
-    out = _empty((M, N), torch.bfloat16, X) if out is None else out
+    if W.shape[1] != K:
+        raise ValueError(_mismatch(locals()))
+    out = _out(out, (M, N), torch.bfloat16, X)
     _check(lib().coda_gemm_rope_fp8(M, N, K, _ptr(X), _ptr(W), float(alpha), _ptr(cos), _ptr(sin), cos.shape[0],
                                     head_dim, rope_cols, _ptr(out), _stream(stream)))
     return out
@@ -589,11 +679,10 @@ def coda_gemm_swiglu_fp8(X, Wgu, alpha: float, want_gu: bool = False, out=None, 
     M, K = X.shape
     F2 = Wgu.shape[0]
     if Wgu.shape[1] != K or F2 % 2:
-        raise ValueError("shape mismatch")
+        raise ValueError(_mismatch(locals()))
     F = F2 // 2
-    out = _empty((M, F), torch.bfloat16, X) if out is None else out
-    if want_gu and gu is None:
-        gu = _empty((M, F2), torch.bfloat16, X)
+    out = _out(out, (M, F), torch.bfloat16, X)
+    gu = _out(gu, (M, F2), torch.bfloat16, X, "gu") if (want_gu or gu is not None) else None
     _check(lib().coda_gemm_swiglu_fp8(M, F, K, _ptr(X), _ptr(Wgu), float(alpha), _ptr(out), _ptr(gu),
                                       _stream(stream)))
     return out, gu
@@ -605,7 +694,7 @@ def coda_gemm_ce_lse_fp8(H, W, alpha: float, labels, with_argmax: bool = True, s
     M, K = H.shape
     V = W.shape[0]
     if W.shape[1] != K or labels.shape[0] != M:
-        raise ValueError("shape mismatch")
+        raise ValueError(_mismatch(locals()))
     nb = coda_num_col_tiles(V)
     pmax = _empty((M, nb), torch.float32, H)
     psum = _empty((M, nb), torch.float32, H)
@@ -618,10 +707,12 @@ def coda_gemm_ce_lse_fp8(H, W, alpha: float, labels, with_argmax: bool = True, s
 
 def coda_gemm_ce_bwd_fp8(H, W, alpha: float, labels, lse, grad_scale: float, out=None, stream=None):
     H, W = _e4m3(H, "H"), _e4m3(W, "W")
-    _i32(labels, "labels"), _f32(lse, "lse")
     M, K = H.shape
     V = W.shape[0]
-    out = _empty((M, V), torch.bfloat16, H) if out is None else out
+    if W.shape[1] != K:
+        raise ValueError(_mismatch(locals()))
+    _i32(labels, "labels", (M,)), _f32(lse, "lse", (M,))
+    out = _out(out, (M, V), torch.bfloat16, H)
     _check(lib().coda_gemm_ce_bwd_fp8(M, V, K, _ptr(H), _ptr(W), float(alpha), _ptr(labels), _ptr(lse),
                                       float(grad_scale), _ptr(out), _stream(stream)))
     return out
