@@ -2,6 +2,8 @@
 // epilogues (pith page, Figure 4 caption: a small kernel reads a few partial
 // values per tile instead of the full activation), plus the RoPE tables.
 // All are HBM/latency bound; one warp per row, coalesced over the partials.
+// They are launched with programmatic dependent launch (light_launch.cuh), so
+// their launch and block scheduling overlap the tail of the GEMM before them.
 #include "host.h"
 #include "light_launch.cuh"
 
