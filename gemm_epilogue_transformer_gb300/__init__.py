@@ -132,8 +132,7 @@ def coda_set_wait_timeout_ns(ns: int):
 
 
 def coda_set_cta_group(g: int):
-    """0 = automatic, 1 = single-SM 128 x 256 tiles, 2 = SM-pair 256 x 256 tiles,
-    4 = two SM pairs per cluster sharing their A rows by multicast."""
+    """0 = automatic, 1 = single-SM 128 x 256 tiles, 2 = SM-pair 256 x 256 tiles."""
     _check(lib().coda_set_cta_group(int(g)))
 
 

@@ -52,10 +52,7 @@ constexpr int kMaxInSlots = 4;
 // Per-variant constants. kCG = 1: one SM computes a 128 x 256 tile. kCG = 2:
 // an SM pair (cta_group::2) computes a 256 x 256 tile; each CTA holds its 128
 // rows of A and half (128 columns) of B, so a stage is 32 KiB per SM instead
-// of 48 KiB. kCG = 4: a cluster of two SM pairs computes two 256 x 256 tiles
-// side by side in N; both pairs need the same A rows, so each CTA loads half
-// of its 128 A rows and multicasts them to its counterpart in the other pair
-// (a quarter less operand traffic from L2 per SM).
+// of 48 KiB.
 // kIn = input boxes per chunk (0, 1, 2), kInWarp = bytes of each epilogue
 // warp's input ring, kSlots = store boxes per staging buffer (1-3), kBufs =
 // staging buffers, kShared = bytes of an epilogue-wide table. The mainloop gets
@@ -64,11 +61,10 @@ constexpr int kMaxInSlots = 4;
 // inputs, 5 / 3 with an 8 KiB ring per warp or three staging boxes.
 template <int kCG, int kIn, int kSlots, int kInWarp = kInWarpBytes, int kBufs = kEpiBufs, int kShared = 0>
 struct Cfg {
-  static constexpr int kPair = kCG == 1 ? 1 : 2;  // CTAs per MMA (cta_group)
-  static constexpr int kPairs = kCG / kPair;       // MMA groups per cluster (1, or 2 sharing A)
+  static_assert(kCG == 1 || kCG == 2, "single-SM or SM-pair tiles");
+  static constexpr int kPair = kCG;               // CTAs per MMA (cta_group)
   static constexpr int kTileM = BM * kPair;
-  static constexpr int kBLoad = BN / kPair;        // B columns loaded per CTA
-  static constexpr int kALoadRows = BM / kPairs;   // A rows each CTA fetches from global memory
+  static constexpr int kBLoad = BN / kPair;       // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = kBLoad * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -82,7 +78,7 @@ struct Cfg {
   static constexpr int kFixedBytes = 1024 + kEpiWarps * kEpiWarpBytes + kInBytes + kShared + 16 +
                                      8 * (2 + 2 + 1 + kEpiWarps * kMaxInSlots);
   static constexpr int kFitStages = (232448 - kFixedBytes) / (kStageBytes + 16);
-  static constexpr int kMaxStages = kCG >= 2 ? 6 : 4;
+  static constexpr int kMaxStages = kCG == 2 ? 6 : 4;
   static constexpr int kStages = kFitStages < kMaxStages ? kFitStages : kMaxStages;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
   static constexpr int kSmemBytes =
@@ -166,20 +162,17 @@ struct EpiCtx {
 // Tile order: groups of group_m row-blocks sweep all column blocks, so the
 // A rows of a group and the B columns in flight stay L2 resident.
 __device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_blk, int& n_blk);
-// Work item t -> row block, first column and width (256 or 128 columns) of
-// MMA group `pr` of kPairs. With two groups a column block is 2 x 256 wide
-// and group pr takes its pr-th 256 (or, in a half item, 128) columns.
-template <int kPairs = 1>
-__device__ __forceinline__ void item_coords(int t, const GemmShape& p, int pr, int& m_blk, int& n0, int& ncols) {
+// Work item t -> row block, first column and width (256 or 128 columns).
+__device__ __forceinline__ void item_coords(int t, const GemmShape& p, int& m_blk, int& n0, int& ncols) {
   int n_blk;
   if (t < p.full_items) {
     tile_coords(t, p, m_blk, n_blk);
-    n0 = n_blk * BN * kPairs + pr * BN;
+    n0 = n_blk * BN;
     ncols = BN;
   } else {
     const int h = t - p.full_items;
     tile_coords(p.full_items + (h >> 1), p, m_blk, n_blk);
-    n0 = n_blk * BN * kPairs + (h & 1) * BSEG * kPairs + pr * BSEG;
+    n0 = n_blk * BN + (h & 1) * BSEG;
     ncols = BSEG;
   }
 }
@@ -335,13 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t s_base = smem_u32(smem);
   // In a pair, the even CTA (the leader) issues the MMAs for both; its full
-  // and TMEM-empty barriers collect the pair's arrivals. With two pairs per
-  // cluster, pr is this CTA's pair and q its place in the pair.
-  constexpr int kPair = C::kPair, kPairs = C::kPairs;
-  const uint32_t rank = kCG >= 2 ? cluster_ctarank() : 0u;
-  const uint32_t q = rank & 1u;
-  const int pr = static_cast<int>(rank >> 1);
-  const uint32_t leader_rank = rank & ~1u;
+  // and TMEM-empty barriers collect the pair's arrivals. q is this CTA's place
+  // in the pair.
+  constexpr int kPair = C::kPair;
+  const uint32_t q = kCG == 2 ? cluster_ctarank() : 0u;
+  constexpr uint32_t leader_rank = 0u;
   const bool leader = q == 0;
   const int cluster_id = blockIdx.x / kCG;
   const int num_clusters = gridDim.x / kCG;
@@ -355,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kPairs);  // a stage is free once every pair that reads it is done
+      mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -371,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tmB);
   }
   if (warp == 1) {
-    if constexpr (kCG >= 2) {
+    if constexpr (kCG == 2) {
       tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
       tmem_relinquish_pair();
     } else {
@@ -381,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (kCG >= 2) cluster_sync_all();  // barriers of all CTAs initialised before any remote signal
+  if constexpr (kCG == 2) cluster_sync_all();  // barriers of all CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // The prologue above (barriers, TMEM, tensor-map prefetch) touches no global
@@ -405,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int t = cluster_id; t < p.num_items && ok; t += num_clusters) {
         int m_blk, n0, ncols;
-        item_coords<kPairs>(t, p, pr, m_blk, n0, ncols);
+        item_coords(t, p, m_blk, n0, ncols);
         const int m0 = m_blk * C::kTileM + static_cast<int>(q) * BM;
         const int bcols = ncols / kPair;  // B columns this CTA loads
         const int nb0 = n0 + static_cast<int>(q) * bcols;
@@ -423,35 +414,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = full_bar(stage);
           if (leader) mbar_arrive_expect_tx(fb, tx);
-          const uint32_t fb_target = kCG >= 2 ? mapa_shared(fb, leader_rank) : fb;
+          const uint32_t fb_target = kCG == 2 ? mapa_shared(fb, leader_rank) : fb;
           const uint32_t a_dst = s_base + stage * C::kStageBytes;
           const uint32_t b_dst = a_dst + C::kABytes;
           const int k0 = kb * (kF8 ? 2 * BK : BK);  // elements: one 128-byte row per stage either way
           auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
-            if constexpr (kCG >= 2)
+            if constexpr (kCG == 2)
               tma_load_2d_pair(dst, m, fb_target, x, y);
             else
               tma_load_2d(dst, m, fb_target, x, y);
           };
           auto load3 = [&](uint32_t dst, const CUtensorMap* m, int y, int z) {
-            if constexpr (kCG >= 2)
+            if constexpr (kCG == 2)
               tma_load_3d_pair(dst, m, fb_target, 0, y, z);
             else
               tma_load_3d(dst, m, fb_target, 0, y, z);
           };
-          if constexpr (kPairs == 2) {
-            // this CTA's 64-row half of the A rows it shares with its
-            // counterpart in the other pair, to both CTAs
-            const uint16_t mask = static_cast<uint16_t>(0x5u << q);
-            const uint32_t dst = a_dst + pr * 8192;
-            const int ma = m0 + 64 * pr;
-            if (p.a_mn == 2)
-              tma_load_3d_pair_mc(dst, &tmA, fb_target, 0, k0, ma >> 6, mask);
-            else if (p.a_mn)
-              tma_load_2d_pair_mc(dst, &tmA, fb_target, ma, k0, mask);
-            else
-              tma_load_2d_pair_mc(dst, &tmA, fb_target, k0, ma, mask);
-          } else if (p.a_mn == 2) {
+          if (p.a_mn == 2) {
             load3(a_dst, &tmA, k0, m0 >> 6);
           } else if (p.a_mn) {
             load(a_dst, &tmA, m0, k0);
@@ -476,9 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Drain: every load signalled on this CTA's full barriers has landed
-      // before the CTA exits (in a pair, all loads signal the leader's; with
-      // two pairs, the other pair's multicast halves too, in lock step). Fill
-      // f of stage s completes phase (f / kStages) & 1 of that stage's barrier.
+      // before the CTA exits (in a pair, both CTAs' loads signal the leader's,
+      // in lock step). Fill f of stage s completes phase (f / kStages) & 1 of
+      // that stage's barrier.
       if (leader)
         for (int s = 0; s < C::kStages; ++s) {
           const uint32_t fills = issued / C::kStages + (static_cast<uint32_t>(s) < issued % C::kStages ? 1u : 0u);
@@ -524,21 +503,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024u);
             const uint32_t acc_in = (kb > 0 || k > 0) ? 1u : 0u;
             if constexpr (kF8) {
-              if constexpr (kCG >= 2)
+              if constexpr (kCG == 2)
                 tc_mma_f8_pair(d_tmem, ad, bd, idesc, acc_in);
               else
                 tc_mma_f8(d_tmem, ad, bd, idesc, acc_in);
             } else {
-              if constexpr (kCG >= 2)
+              if constexpr (kCG == 2)
                 tc_mma_bf16_pair(d_tmem, ad, bd, idesc, acc_in);
               else
                 tc_mma_bf16(d_tmem, ad, bd, idesc, acc_in);
             }
           }
-          // the stage is free in every CTA this pair's MMAs read from (with two
-          // pairs, all four: each CTA's A half also lands in the other pair)
-          if constexpr (kCG >= 2)
-            tc_commit_pair(empty_bar(stage), kPairs == 2 ? 0xF : 0x3);
+          // the stage is free in both CTAs of the pair
+          if constexpr (kCG == 2)
+            tc_commit_pair(empty_bar(stage), 0x3);
           else
             tc_commit(empty_bar(stage));
           if (++stage == C::kStages) {
@@ -547,13 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if constexpr (kCG >= 2)
+        if constexpr (kCG == 2)
           tc_commit_pair(tfull_bar(buf), static_cast<uint16_t>(0x3u << leader_rank));
         else
           tc_commit(tfull_bar(buf));
       }
       // Drain: all MMAs issued here complete before TMEM is freed.
-      if constexpr (kCG >= 2)
+      if constexpr (kCG == 2)
         tc_commit_pair(drain_bar, static_cast<uint16_t>(1u << leader_rank));
       else
         tc_commit(drain_bar);
@@ -575,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Segment `seg` (128 columns) of work item tt; false if it lies past N.
     auto make_ctx = [&](int tt, int seg, EpiCtx& cx) {
       int n0, ncols;
-      item_coords<kPairs>(tt, p, pr, cx.m_blk, n0, ncols);
+      item_coords(tt, p, cx.m_blk, n0, ncols);
       cx.M = p.M;
       cx.N = p.N;
       cx.m0 = cx.m_blk * C::kTileM + static_cast<int>(q) * BM;
@@ -727,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (kCG >= 2)
+        if constexpr (kCG == 2)
           mbar_arrive_remote(mapa_shared(tempty_bar(buf), leader_rank));
         else
           mbar_arrive(tempty_bar(buf));
@@ -746,10 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // In a pair, neither CTA releases TMEM (or its shared memory) while the
   // leader's MMAs may still read or write it.
-  if constexpr (kCG >= 2) cluster_sync_all();
+  if constexpr (kCG == 2) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (kCG >= 2)
+    if constexpr (kCG == 2)
       tmem_dealloc_pair(tmem_base, kTmemCols);
     else
       tmem_dealloc(tmem_base, kTmemCols);

@@ -60,17 +60,17 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   if (b_mn && N % 64 == 0) b_mn = 2;
   if (kF8 && K > 0) {
     if (a_mn || b_mn) return fail(CODA_ERR_UNSUPPORTED, "%s: FP8 operands must be K-major", fn);
-    rc = make_map_u8(&tA, A, K, M, static_cast<uint64_t>(lda), 2 * BK, C::kALoadRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    rc = make_map_u8(&tA, A, K, M, static_cast<uint64_t>(lda), 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     rc = make_map_u8(&tB, B, K, N, static_cast<uint64_t>(ldb), 2 * BK, C::kBLoad, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   } else if (K > 0) {
     if (a_mn == 2)
-      rc = make_map_bf16_mn3d(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, C::kALoadRows / 64);
+      rc = make_map_bf16_mn3d(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, BM / 64);
     else if (a_mn)
       rc = make_map_bf16(&tA, A, M, K, static_cast<uint64_t>(lda) * 2u, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     else
-      rc = make_map_bf16(&tA, A, K, M, static_cast<uint64_t>(lda) * 2u, 64, C::kALoadRows,
+      rc = make_map_bf16(&tA, A, K, M, static_cast<uint64_t>(lda) * 2u, 64, BM,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     if (b_mn == 2)
@@ -120,7 +120,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.m_blocks = (M + C::kTileM - 1) / C::kTileM;
-  p.n_blocks = (N + BN * C::kPairs - 1) / (BN * C::kPairs);  // column blocks of kPairs tiles
+  p.n_blocks = (N + BN - 1) / BN;
   p.k_blocks = kF8 ? (K + 2 * BK - 1) / (2 * BK) : (K + BK - 1) / BK;
   p.num_tiles = p.m_blocks * p.n_blocks;
   // Raster group: the row blocks that sweep all column blocks together (tile
@@ -138,7 +138,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   // Wave balance: a last wave of `rem` tiles that fills at most half of the
   // persistent clusters runs as 2 * rem half tiles (256 x 128 per pair) instead.
   const int rem = p.num_tiles % cmax;
-  if (rem > 0 && 2 * rem <= cmax && N > BSEG * C::kPairs) {
+  if (rem > 0 && 2 * rem <= cmax && N > BSEG) {
     p.full_items = p.num_tiles - rem;
     p.num_items = p.num_tiles + rem;
   } else {
@@ -165,9 +165,9 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   return CODA_OK;
 }
 
-// One persistent CTA (kCG = 1), CTA pair (kCG = 2) or pair of pairs (kCG = 4)
-// per SM / SM pair / four SMs. The pair variant is used once M spans more than
-// one 128-row block, unless coda_set_cta_group() fixed the choice.
+// One persistent CTA (kCG = 1) or CTA pair (kCG = 2) per SM / SM pair. The
+// pair variant is used once M spans more than one 128-row block, unless
+// coda_set_cta_group() fixed the choice.
 // o0 / o1: TMA store targets; i0 / i1: TMA sources of the epilogue's input
 // boxes (unused maps may be any valid map).
 template <class Epi, bool kF8 = false>
@@ -178,9 +178,6 @@ int launch_fused(const char* fn, int M, int N, int K, const void* A, int lda, in
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int forced = cta_group_setting();
   const int g = forced ? forced : (M > BM ? 2 : 1);
-  if (g == 4)
-    return launch_variant<Epi, 4, kF8>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream,
-                                       alpha);
   if (g == 2)
     return launch_variant<Epi, 2, kF8>(fn, di, M, N, K, A, lda, a_mn, B, ldb, b_mn, o0, o1, i0, i1, ep, stream,
                                        alpha);

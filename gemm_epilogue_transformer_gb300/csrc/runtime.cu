@@ -192,7 +192,7 @@ int coda_set_wait_timeout_ns(unsigned long long ns) {
 }
 
 int coda_set_cta_group(int g) {
-  if (g < 0 || g > 4 || g == 3) return fail(CODA_ERR_INVALID, "coda_set_cta_group: %d is not 0, 1, 2 or 4", g);
+  if (g < 0 || g > 2) return fail(CODA_ERR_INVALID, "coda_set_cta_group: %d is not 0, 1 or 2", g);
   g_cta_group = g;
   return CODA_OK;
 }

@@ -83,9 +83,7 @@ int coda_set_wait_timeout_ns(unsigned long long ns);
 
 /* GEMM tile variant for every later launch on this process: 1 = one SM per
  * 128 x 256 tile (tcgen05 cta_group::1); 2 = an SM pair per 256 x 256 tile
- * (cta_group::2, 2-CTA clusters); 4 = two SM pairs per 4-CTA cluster on two
- * 256 x 256 tiles that share their A rows, each A half fetched once and
- * multicast to both pairs; 0 (default) = the pair whenever M > 128.
+ * (cta_group::2, 2-CTA clusters); 0 (default) = the pair whenever M > 128.
  * Results are identical up to fp32 accumulation order. Other values are
  * rejected with CODA_ERR_INVALID. */
 int coda_set_cta_group(int g);

@@ -45,7 +45,7 @@ def assert_chain(got, ref, name):
     assert fro <= CHAIN_FRO and mx <= CHAIN_MAX, f"{name}: chain rel Frobenius {fro:.3e}, scaled max {mx:.3e}"
 
 
-@pytest.fixture(params=[0, 1, 4], ids=["auto", "cta1", "cta4"])
+@pytest.fixture(params=[0, 1], ids=["auto", "cta1"])
 def cta_group(coda, request):
     coda.coda_set_cta_group(request.param)
     yield request.param

@@ -29,7 +29,7 @@ def _ops(M, K, N, seed, labels=False):
     return p, a, b, p["sA"] * p["sB"]
 
 
-@pytest.fixture(params=[1, 2, 4], ids=["cta1", "cta2", "cta4"])
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
 def cta_group(coda, request):
     coda.coda_set_cta_group(request.param)
     yield request.param

@@ -15,7 +15,7 @@ PAD = 32  # padding rows after each output
 INT_SENTINEL = -7
 
 
-@pytest.fixture(params=[1, 2, 4], ids=["cta1", "cta2", "cta4"])
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
 def cta_group(coda, request):
     coda.coda_set_cta_group(request.param)
     yield request.param
