@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config fused/unfused entries of the default run")
     ap.add_argument("--suite", action="store_true",
                     help="time every fused operator against its unfused pair on all five workloads "
                          "(one JSON line per operator) instead of the headline step")
@@ -158,12 +160,69 @@ class Clocks:
                 if any(r[3].replace(".", "").isdigit() for r in rows) else None}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons polled through NVML (ctypes, read-only
+    queries) every few milliseconds on a host thread, for timed regions too
+    short for the nvidia-smi sampler. Unavailable NVML leaves it empty."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index):
+        import ctypes
+        import threading
+        self.samples, self.reasons, self.h, self.nv = [], 0, None, None
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            h = ctypes.c_void_p()
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h = nv, h
+        except (OSError, AttributeError, RuntimeError):
+            self.nv = None
+
+    def _poll(self):
+        import ctypes
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:  # 1 = SM clock
+                self.samples.append(mhz.value)
+            if self.nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            self._stop.wait(0.002)
+
+    def start(self):
+        if self.nv is not None:
+            import threading
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def stop(self):
+        if self._t is not None:
+            self._stop.set()
+            self._t.join()
+        if not self.samples:
+            return {"sm_mhz": None, "samples": 0, "source": "nvml unavailable"}
+        return {"sm_mhz": float(np.median(self.samples)), "sm_mhz_min": float(min(self.samples)),
+                "samples": len(self.samples), "source": "nvml, 2 ms polling",
+                "reasons": sorted(v for k, v in self.REASONS.items() if self.reasons & k)}
+
+
 def measured_peaks():
+    """(burst bf16 TFLOP/s, sustained bf16 TFLOP/s, HBM GB/s, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return d["bf16_tflops"], d["hbm_gbs"], "measured"
-    return 1900.0, 6800.0, "fallback"
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
 
 
 # The sources that define the fused RoPE kernel and its launch: the committed
@@ -287,6 +346,7 @@ def main():
         barrier()
         step_ms = [s.elapsed_time(e) for s, e in ev]
         k_ms = [s.elapsed_time(e) for s, e in kev] if kernel_events else None
+        timed.last = (step_ms, k_ms)
         return float(np.mean(step_ms)), (float(np.mean(k_ms)) if k_ms else None)
 
     clocks = Clocks(local)
@@ -300,11 +360,27 @@ def main():
     # NVTX ranges name the phases for profilers (ncu --nvtx --nvtx-include "fused/")
     nvtx = torch.cuda.nvtx
     nvtx.range_push("fused")
+    clk_fused = NvmlClocks(local).start()
     ms_fused, ms_rope = timed(lambda ev: fused_step(X, W, A, B, ev), a.steps, kernel_events=True)
+    clk_fused = clk_fused.stop()
+    step_ms_all, rope_ms_all = timed.last
     nvtx.range_pop()
     nvtx.range_push("unfused")
     ms_unfused, _ = timed(lambda ev: unfused_step(), a.steps)
     nvtx.range_pop()
+
+    # The headline kernel back to back with no L2 flush in between (its inputs,
+    # 128 MiB, then partly stay in the 126 MiB L2): the other cache regime.
+    ev_u = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    for _ in range(3):
+        G.coda_gemm_rope(X, W, cos, sin, hd, rc, out=out)
+    barrier()
+    for s_, e_ in ev_u:
+        s_.record(stream)
+        G.coda_gemm_rope(X, W, cos, sin, hd, rc, out=out)
+        e_.record(stream)
+    barrier()
+    ms_rope_unflushed = float(np.median([s_.elapsed_time(e_) for s_, e_ in ev_u]))
 
     # End to end through the public API: every step copies its four inputs from
     # pinned host memory to the device, runs the step, and copies its three
@@ -392,8 +468,9 @@ def main():
             dist.destroy_process_group()
         return 0
 
-    peak_tf, _, peak_kind = measured_peaks()
+    peak_tf, peak_tf_sus, _, peak_kind = measured_peaks()
     achieved = FLOPS_PER_GEMM / (ms_rope * 1e-3) / 1e12
+    ach_unflushed = FLOPS_PER_GEMM / (ms_rope_unflushed * 1e-3) / 1e12
     traffic = ncu_traffic("coda_gemm_rope")
     line = {
         "metric": METRIC,
@@ -403,6 +480,7 @@ def main():
         "steps": a.steps,
         "warmup": a.warmup,
         "ms_per_step": ms_fused,
+        "ms_per_step_median": float(np.median(step_ms_all)),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -422,9 +500,25 @@ def main():
         "roofline": {"kernel": "coda_gemm_rope (gemm_epilogue_kernel<EpiRope<1>>)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "peak_source": f"bf16_tflops (burst) of {peak_kind}", "traffic": traffic,
-                     "ms_per_launch": ms_rope},
+                     "ms_per_launch": ms_rope, "ms_per_launch_median": float(np.median(rope_ms_all)),
+                     "peak_sustained": peak_tf_sus, "frac_sustained": achieved / peak_tf_sus,
+                     "sm_mhz": clk_fused.get("sm_mhz"), "clock": clk_fused,
+                     "unflushed": {"ms_per_launch": ms_rope_unflushed, "achieved": ach_unflushed,
+                                   "frac": ach_unflushed / peak_tf, "launches": a.steps,
+                                   "l2": "no flush between back-to-back launches"}},
         "device_status": status,
     }
+    if not a.no_configs and world == 1:
+        # every other config, fused against unfused (median of alternating reps)
+        del host, d_in, d_out, h_res, flush
+        torch.cuda.empty_cache()
+        R = Runner(G, dev, reps=20)
+        entries = []
+        for name in CONFIG_WORKLOADS:
+            entries += run_workload(R, name)
+        line["configs"] = {f"{e['workload']}/{e['op']}": e for e in entries}
+        status |= G.coda_device_status(clear=True)
+        line["device_status"] = status
     if not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(line), flush=True)
@@ -464,183 +558,204 @@ def reference_arm(a, rank, world):
 
 # ---------------------------------------------------------------- operator suite
 
-def suite(a):
-    """Fused vs unfused time of every operator on the five workloads; one JSON line each."""
-    import torch
-    import coda_inputs as gen
-    from gemm_epilogue_transformer_gb300 import build_lib
-    build_lib.build()
-    import gemm_epilogue_transformer_gb300 as G
-    G.coda_init(0)
-    dev = torch.device("cuda", 0)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    peak_tf, peak_bw, peak_kind = measured_peaks()
+class Runner:
+    """Times fused sequences against their unfused twins. Repetitions of the
+    two (and of the dominant kernel alone) alternate, with the L2 flushed
+    before every one, so clock and power drift over the run affect every
+    column alike. Each entry samples the SM clock while it runs."""
 
-    def d(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+    def __init__(self, G, dev, reps, min_s=1.0, max_reps=2000):
+        import torch
+        self.G, self.dev, self.reps, self.min_s, self.max_reps = G, dev, reps, min_s, max_reps
+        self.stream = torch.cuda.current_stream(dev)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.peak_tf, self.peak_tf_sus, self.peak_bw, self.peak_kind = measured_peaks()
 
-    def graph_of(fn):
-        """Capture fn's launches into a CUDA graph (after one direct run) and return its replay."""
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            fn()
-        stream.wait_stream(side)
-        torch.cuda.synchronize(dev)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=side):
-            fn()
-        graphs.append(g)
-        return g.replay
+    def _time(self, fns, reps):
+        import torch
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fns]
+              for _ in range(reps)]
+        torch.cuda.synchronize(self.dev)
+        for r in range(reps):
+            for (s, e), fn in zip(ev[r], fns):
+                self.flush.zero_()
+                s.record(self.stream)
+                fn()
+                e.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [[ev[r][i][0].elapsed_time(ev[r][i][1]) for r in range(reps)] for i in range(len(fns))]
 
-    graphs = []
+    def roofline(self, ms, flops, nbytes, peak_mult=1.0):
+        """Fraction of the kernel's roofline: max(F / P, B / BW) / t, against
+        the burst and the sustained bf16 peak (times peak_mult for FP8)."""
+        t_hbm = nbytes / (self.peak_bw * 1e9) if nbytes else 0.0
+        out = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12 if flops else None,
+               "gbs": nbytes / (ms * 1e-3) / 1e9 if nbytes else None}
+        for key, pk in (("frac", self.peak_tf), ("frac_sustained", self.peak_tf_sus)):
+            t_tc = flops / (pk * peak_mult * 1e12) if flops else 0.0
+            out[key] = max(t_tc, t_hbm) / (ms * 1e-3)
+        out["bound"] = "tensor" if flops and flops / (self.peak_tf * peak_mult * 1e12) >= t_hbm else "hbm"
+        return out
 
-    def once(fn):
-        flush.zero_()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        fn()
-        e.record(stream)
-        e.synchronize()
-        return s.elapsed_time(e)
-
-    def report(workload, op, flops, fused, unfused, launches, peak_mult=1.0):
-        # fused and unfused repetitions alternate, so clock and power drift over
-        # the run affect both columns alike
+    def entry(self, workload, op, flops, fused, unfused, launches, kernels=(), peak_mult=1.0, fused_bytes=None):
+        """kernels: (name, fn, flops, bytes) of the sequence's dominant kernel(s),
+        each timed alone; an empty list means `fused` is one kernel (its bytes
+        in fused_bytes)."""
+        fns = [fused, unfused] + [k[1] for k in kernels]
         for _ in range(3):
-            fused()
-            unfused()
-        tf, tu = [], []
-        for _ in range(a.reps):
-            tf.append(once(fused))
-            tu.append(once(unfused))
-        fm, fmin = float(np.median(tf)), float(np.min(tf))
-        um, umin = float(np.median(tu)), float(np.min(tu))
-        pk = peak_tf * peak_mult
-        line = {"suite": workload, "op": op, "fused_ms": fm, "fused_min_ms": fmin, "unfused_ms": um,
-                "unfused_min_ms": umin, "speedup_vs_unfused": um / fm,
-                "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None,
-                "pct_bf16_peak": 100 * flops / (fm * 1e-3) / 1e12 / pk if flops else None,
-                "kernels": launches, "reps": a.reps,
-                "peak": (f"{pk:.1f} TFLOP/s ({peak_kind} bf16 x {peak_mult:g})" if peak_mult != 1.0
-                         else f"{peak_tf} TFLOP/s ({peak_kind})")}
-        print(json.dumps(line), flush=True)
-
-    # -- GEMM-RMSNorm-GEMM (tiny and 8192)
-    def want(name):
-        return a.only is None or a.only == name
-
-    for name, M, Kd, bwdK in (("rmsnorm_chain_tiny", 256, 512, 512), ("rmsnorm_chain_8192", 8192, 8192, 8192)):
-        if not want(name):
-            continue
-        p = gen.rms_chain(M, Kd, Kd, Kd, seed=0, bwd_K=bwdK)
-        x, W0, z, g, W1, dO, Wn = (d(p[k]) for k in ("x", "W0", "z", "gamma", "W1", "dO", "Wn"))
-        d_ = Kd
-        nb = G.coda_num_col_tiles(d_)
-        h1 = torch.empty((M, d_), dtype=torch.bfloat16, device=dev)
-        h2, h0, n, Y, dY, dYr, Gm, dh1 = (torch.empty_like(h1) for _ in range(8))
-        psq = torch.empty((M, nb), dtype=torch.float32, device=dev)
-        pdot = torch.empty_like(psq)
-        r = torch.empty((M,), dtype=torch.float32, device=dev)
-        ru = torch.empty_like(r)
-
-        def fused_fwd():
-            G.coda_gemm_res_rmsprep(x, W0, z, g, h1=h1, h2=h2, psq=psq)
-            G.coda_rms_reduce(psq, d_, 1e-6, r=r)
-            G.coda_gemm_rowscale(h2, W1, r, out=Y)
-
-        def unfused_fwd():
-            G.coda_gemm(x, W0, out=h0)
-            G.coda_unfused_add(h0, z, out=h1)
-            nn, rr = G.coda_unfused_rmsnorm(h1, g, 1e-6)
-            G.coda_gemm(nn, W1, out=Y)
-
-        report(name, "fwd", 2 * 2.0 * M * Kd * d_, fused_fwd, unfused_fwd, "3 fused (2 GEMM + aux) vs 4 unfused")
-        if M * Kd <= 256 * 512:
-            # the tiny chain is launch-bound: the same sequences replayed from CUDA graphs
-            report(name, "fwd_graph", 2 * 2.0 * M * Kd * d_, graph_of(fused_fwd), graph_of(unfused_fwd),
-                   "the same launches, each sequence replayed from one CUDA graph")
-        fused_fwd()
-
-        def fused_bwd():
-            dY_, dYr_, pd = G.coda_gemm_rowdot(dO, Wn, Y, r)
-            s_ = G.coda_rowdot_reduce(pd, d_)
-            dh, pdg = G.coda_gemm_rmsnorm_bwd(dY_, W1, h1, g, r, s_)
-            G.coda_colsum_reduce(pdg)
-
-        def unfused_bwd():
-            dY_ = G.coda_gemm(dO, Wn)
-            Gd = G.coda_gemm(dY_, W1, transB=True)
-            dh, pdg = G.coda_unfused_rmsnorm_bwd(Gd, h1, g, r)
-            G.coda_colsum_reduce(pdg)
-
-        report(name, "bwd", 2 * 2.0 * M * Kd * d_, fused_bwd, unfused_bwd,
-               "dY GEMM + rowdot + RMSNorm-bwd GEMM + 2 aux vs 2 GEMM + rmsnorm_bwd + colsum")
-        del p, x, W0, z, g, W1, dO, Wn, h1, h2, h0, n, Y, dY, dYr, Gm, dh1
-        torch.cuda.empty_cache()
-
-    # -- GEMM + RoPE
-    M, K, N, hd, rc = 4096, 4096, 12288, 128, 8192
-    if want("rope_qkv_4096"):
-        rope_suite(G, gen, d, dev, report, M, K, N, hd, rc)
-    if want("swiglu_up_4096"):
-        swiglu_suite(G, gen, d, dev, report)
-    if want("lm_head_ce_8192"):
-        ce_suite(G, gen, d, dev, report)
-    for dm in sorted(gen.BLOCK_SIZES):
-        if want(f"block_d{dm}"):
-            block_suite(G, gen, dev, report, dm)
-    fp8_suite(G, gen, dev, report, want)
-    status = G.coda_device_status(clear=True)
-    print(json.dumps({"suite": "done", "device_status": status}), flush=True)
-    return 0 if status == 0 else 1
+            for fn in fns:
+                fn()
+        one = self._time(fns, 1)
+        round_ms = sum(x[0] for x in one) + 0.05 * len(fns)
+        reps = int(min(self.max_reps, max(self.reps, np.ceil(1e3 * self.min_s / round_ms))))
+        clk = NvmlClocks(self.dev.index or 0).start()
+        t = self._time(fns, reps)
+        c = clk.stop()
+        fm, um = float(np.median(t[0])), float(np.median(t[1]))
+        e = {"workload": workload, "op": op, "fused_ms": fm, "fused_min_ms": float(np.min(t[0])),
+             "unfused_ms": um, "unfused_min_ms": float(np.min(t[1])), "speedup_vs_unfused": um / fm,
+             "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None, "reps": reps,
+             "kernels": launches, "sm_mhz": c.get("sm_mhz"), "clock_reasons": c.get("reasons"),
+             "clock_samples": c.get("samples")}
+        if peak_mult != 1.0:
+            e["peak_note"] = f"FP8 peak taken as {peak_mult:g} x the bf16 peak"
+        if kernels:
+            e["dominant"] = []
+            for (name, _, kf, kb), tk in zip(kernels, t[2:]):
+                e["dominant"].append({"kernel": name, **self.roofline(float(np.median(tk)), kf, kb, peak_mult)})
+        else:
+            e["dominant"] = [{"kernel": "the fused kernel", **self.roofline(fm, flops, fused_bytes or 0, peak_mult)}]
+        return e
 
 
-def rope_suite(G, gen, d, dev, report, M, K, N, hd, rc):
+def _dev_normal(gen_t, dev):
     import torch
-    p = gen.rope_problem(M, K, N, seed=0)
-    X, W, A_, B_ = (d(p[k]) for k in ("X", "W", "A", "B"))
+
+    def normal(shape, std=1.0, mean=0.0):
+        x = torch.randn(shape, generator=gen_t, device=dev, dtype=torch.float32)
+        return (x * std + mean).to(torch.bfloat16)
+    return normal
+
+
+def rms_chain_entries(R, name, M, Kd):
+    """GEMM-RMSNorm-GEMM forward and backward (d = N = K = Kd)."""
+    import torch
+    G, dev = R.G, R.dev
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    d_ = Kd
+    x, W0, z = nrm((M, Kd)), nrm((Kd, d_), Kd ** -0.5), nrm((M, d_))
+    gam, W1 = nrm((d_,), 0.1, 1.0), nrm((d_, d_), d_ ** -0.5)
+    dO, Wn = nrm((M, Kd)), nrm((Kd, d_), Kd ** -0.5)
+    nb = G.coda_num_col_tiles(d_)
+    h1 = torch.empty((M, d_), dtype=torch.bfloat16, device=dev)
+    h2, h0, Y = (torch.empty_like(h1) for _ in range(3))
+    psq = torch.empty((M, nb), dtype=torch.float32, device=dev)
+    r = torch.empty((M,), dtype=torch.float32, device=dev)
+
+    def fused_fwd():
+        G.coda_gemm_res_rmsprep(x, W0, z, gam, h1=h1, h2=h2, psq=psq)
+        G.coda_rms_reduce(psq, d_, 1e-6, r=r)
+        G.coda_gemm_rowscale(h2, W1, r, out=Y)
+
+    def unfused_fwd():
+        G.coda_gemm(x, W0, out=h0)
+        G.coda_unfused_add(h0, z, out=h1)
+        nn, _ = G.coda_unfused_rmsnorm(h1, gam, 1e-6)
+        G.coda_gemm(nn, W1, out=Y)
+
+    fl = 2.0 * M * Kd * d_
+    b1 = 2.0 * (M * Kd + Kd * d_ + 3 * M * d_ + d_) + 4.0 * M * nb
+    out = [R.entry(name, "fwd", 2 * fl, fused_fwd, unfused_fwd, "3 fused (2 GEMM + aux) vs 4 unfused",
+                   kernels=[("coda_gemm_res_rmsprep (GEMM1: h1, h2, row partials)",
+                             lambda: G.coda_gemm_res_rmsprep(x, W0, z, gam, h1=h1, h2=h2, psq=psq), fl, b1)])]
+    fused_fwd()
+    st = {}
+
+    def fused_bwd():
+        dY_, _, pd = G.coda_gemm_rowdot(dO, Wn, Y, r)
+        s_ = G.coda_rowdot_reduce(pd, d_)
+        dh, pdg = G.coda_gemm_rmsnorm_bwd(dY_, W1, h1, gam, r, s_)
+        G.coda_colsum_reduce(pdg)
+        st["dY"], st["s"] = dY_, s_
+
+    def unfused_bwd():
+        dY_ = G.coda_gemm(dO, Wn)
+        Gd = G.coda_gemm(dY_, W1, transB=True)
+        _, pdg = G.coda_unfused_rmsnorm_bwd(Gd, h1, gam, r)
+        G.coda_colsum_reduce(pdg)
+
+    fused_bwd()
+    b2 = 2.0 * (M * d_ + d_ * d_ + 2 * M * d_ + d_) + 4.0 * (2 * M + (M // 32 + 1) * d_)
+    out.append(R.entry(name, "bwd", 2 * fl, fused_bwd, unfused_bwd,
+                       "dY GEMM + rowdot + RMSNorm-bwd GEMM + 2 aux vs 2 GEMM + rmsnorm_bwd + colsum",
+                       kernels=[("coda_gemm_rmsnorm_bwd (dgrad of GEMM2: dh1, dgamma partials)",
+                                 lambda: G.coda_gemm_rmsnorm_bwd(st["dY"], W1, h1, gam, r, st["s"]), fl, b2)]))
+    return out
+
+
+def rope_entries(R):
+    import torch
+    G, dev = R.G, R.dev
+    M, K, N, hd, rc = 4096, 4096, 12288, 128, 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    X, W, A_, B_ = nrm((M, K)), nrm((K, N), K ** -0.5), nrm((M, K)), nrm((K, N), K ** -0.5)
     c, sn = G.coda_rope_tables(4096, hd, 10000.0, device=dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    report("rope_qkv_4096", "fwd", 2.0 * M * N * K, lambda: G.coda_gemm_rope(X, W, c, sn, hd, rc, out=out),
-           lambda: (G.coda_gemm(X, W, out=out), G.coda_unfused_rope(out, c, sn, hd, rc)), "1 vs 2")
-    report("rope_qkv_4096", "bwd", 2.0 * M * N * K, lambda: G.coda_gemm_rope_bwd(A_, B_, c, sn, hd, rc, out=out),
-           lambda: (G.coda_gemm(A_, B_, out=out), G.coda_unfused_rope_bwd(out, c, sn, hd, rc)), "1 vs 2")
-    report("rope_qkv_4096", "plain_gemm", 2.0 * M * N * K, lambda: G.coda_gemm(X, W, out=out),
-           lambda: G.coda_gemm(X, W, out=out), "identity epilogue, both columns the same kernel")
-    del p, X, W, A_, B_, out
-    torch.cuda.empty_cache()
+    fl, by = 2.0 * M * N * K, 2.0 * (M * K + K * N + M * N) + 8.0 * 4096 * hd // 2
+    return [R.entry("rope_qkv_4096", "fwd", fl, lambda: G.coda_gemm_rope(X, W, c, sn, hd, rc, out=out),
+                    lambda: (G.coda_gemm(X, W, out=out), G.coda_unfused_rope(out, c, sn, hd, rc)), "1 vs 2",
+                    fused_bytes=by),
+            R.entry("rope_qkv_4096", "bwd", fl, lambda: G.coda_gemm_rope_bwd(A_, B_, c, sn, hd, rc, out=out),
+                    lambda: (G.coda_gemm(A_, B_, out=out), G.coda_unfused_rope_bwd(out, c, sn, hd, rc)), "1 vs 2",
+                    fused_bytes=by),
+            R.entry("rope_qkv_4096", "plain_gemm", fl, lambda: G.coda_gemm(X, W, out=out),
+                    lambda: G.coda_gemm(X, W, out=out), "identity epilogue, both columns the same kernel",
+                    fused_bytes=2.0 * (M * K + K * N + M * N))]
 
 
-def swiglu_suite(G, gen, d, dev, report):
+def swiglu_entries(R):
     import torch
+    G, dev = R.G, R.dev
     M, K, F = 4096, 4096, 14336
-    p = gen.swiglu_problem(M, K, F, seed=0)
-    X, Wgu, dYs, Wd = (d(p[k]) for k in ("X", "Wgu", "dY", "Wd"))
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    X, Wgu, dYs, Wd = nrm((M, K)), nrm((K, 2 * F), K ** -0.5), nrm((M, K)), nrm((F, K), F ** -0.5)
     A = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
     GU = torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev)
     dA = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
     dGU = torch.empty_like(GU)
-    report("swiglu_up_4096", "fwd", 2.0 * M * 2 * F * K, lambda: G.coda_gemm_swiglu(X, Wgu, out=A),
-           lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (no GU saved)")
-    report("swiglu_up_4096", "fwd_save_gu", 2.0 * M * 2 * F * K,
-           lambda: G.coda_gemm_swiglu(X, Wgu, out=A, gu=GU),
-           lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (GU saved for backward)")
-    report("swiglu_up_4096", "bwd", 2.0 * M * F * K, lambda: G.coda_gemm_swiglu_bwd(dYs, Wd, GU, out=dGU),
-           lambda: (G.coda_gemm(dYs, Wd, transB=True, out=dA), G.coda_unfused_swiglu_bwd(dA, GU)), "1 vs 2")
-    del p, X, Wgu, dYs, Wd, A, GU, dA, dGU
-    torch.cuda.empty_cache()
+    fl = 2.0 * M * 2 * F * K
+    by = 2.0 * (M * K + K * 2 * F + M * F)
+    out = [R.entry("swiglu_up_4096", "fwd", fl, lambda: G.coda_gemm_swiglu(X, Wgu, out=A),
+                   lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (no GU saved)",
+                   fused_bytes=by),
+           R.entry("swiglu_up_4096", "fwd_save_gu", fl, lambda: G.coda_gemm_swiglu(X, Wgu, out=A, gu=GU),
+                   lambda: (G.coda_gemm(X, Wgu, out=GU), G.coda_unfused_swiglu(GU)),
+                   "1 vs 2 (GU saved for backward)", fused_bytes=by + 2.0 * M * 2 * F)]
+    G.coda_gemm_swiglu(X, Wgu, out=A, gu=GU)
+    out.append(R.entry("swiglu_up_4096", "bwd", fl / 2, lambda: G.coda_gemm_swiglu_bwd(dYs, Wd, GU, out=dGU),
+                       lambda: (G.coda_gemm(dYs, Wd, transB=True, out=dA), G.coda_unfused_swiglu_bwd(dA, GU)),
+                       "1 vs 2", fused_bytes=2.0 * (M * K + F * K + 2 * M * 2 * F)))
+    return out
 
 
-def ce_suite(G, gen, d, dev, report):
+def ce_entries(R):
     import torch
+    G, dev = R.G, R.dev
     M, K, V = 8192, 4096, 32768
-    p = gen.ce_problem(M, K, V, seed=0)
-    H, W = d(p["H"]), d(p["W"])
-    y = torch.from_numpy(p["labels"]).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    H, W = nrm((M, K)), nrm((K, V), K ** -0.5)
+    y = torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
     logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
     st = {}
+    nb = G.coda_num_col_tiles(V)
 
     def fused_ce():
         pm, ps, pa, tg = G.coda_gemm_ce_lse(H, W, y)
@@ -650,20 +765,74 @@ def ce_suite(G, gen, d, dev, report):
         G.coda_gemm(H, W, out=logits)
         G.coda_unfused_ce_fwd(logits, y)
 
-    report("lm_head_ce_8192", "fwd", 2.0 * M * V * K, fused_ce, unfused_ce, "GEMM+partials + reduce vs GEMM (bf16 logits) + CE")
+    fl = 2.0 * M * V * K
+    b_in = 2.0 * (M * K + K * V) + 4.0 * M
+    out = [R.entry("lm_head_ce_8192", "fwd", fl, fused_ce, unfused_ce,
+                   "GEMM+partials + reduce vs GEMM (bf16 logits) + CE",
+                   kernels=[("coda_gemm_ce_lse (online LSE partials)", lambda: G.coda_gemm_ce_lse(H, W, y), fl,
+                             b_in + 12.0 * M * nb + 4.0 * M)])]
     fused_ce()
     lse = st["lse"]
-    report("lm_head_ce_8192", "bwd_dlogits", 2.0 * M * V * K,
-           lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
-           lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
-           "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel")
+    out.append(R.entry("lm_head_ce_8192", "bwd_dlogits", fl,
+                       lambda: G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=logits),
+                       lambda: (G.coda_gemm(H, W, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / M)),
+                       "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel",
+                       fused_bytes=b_in + 4.0 * M + 2.0 * M * V))
+    return out
 
 
-def fp8_suite(G, gen, dev, report, want):
+def block_entries(R, dm):
+    """One period of the block-level chain (RoPE-path and SwiGLU-path
+    GEMM-residual-RMSNorm-GEMM structures) at 16K tokens, forward and forward +
+    backward, fused sequence vs unfused sequence."""
+    import torch
+    import coda_inputs as gen
+    G, dev = R.G, R.dev
+    c = gen.WORKLOADS[f"block_d{dm}"]
+    M, d, F, hd, rc, S = c["M"], c["d"], c["F"], c["head_dim"], c["rope_cols"], c["S"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    t = dict(P=nrm((M, F)), Wd=nrm((F, d), F ** -0.5), x=nrm((M, d)), gamma1=nrm((d,), 0.1, 1.0),
+             Wqkv=nrm((d, 3 * d), d ** -0.5), O=nrm((M, d)), Wo=nrm((d, d), d ** -0.5),
+             gamma2=nrm((d,), 0.1, 1.0), Wgu=nrm((d, 2 * F), d ** -0.5), dQKV=nrm((M, 3 * d)),
+             gh=nrm((M, d)), Wdn=nrm((F, d), F ** -0.5))
+    cos, sin = G.coda_rope_tables(S, hd, c["theta"], device=dev)
+    fl_fwd = 2.0 * M * d * (3 * F + 4 * d)
+    fused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"])
+    unfused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"], unfused=True)
+    name = f"block_d{dm}"
+    fl_up = 2.0 * M * d * 2 * F
+    up_bytes = 2.0 * (M * d + d * 2 * F + M * F + M * 2 * F) + 4.0 * M
+    out = [R.entry(name, "fwd", fl_fwd, fused.fwd, unfused.fwd_unfused, "6 fused launches vs 10 unfused",
+                   kernels=[("coda_gemm_rowscale_swiglu (SwiGLU up-projection, GU saved)",
+                             lambda: G.coda_gemm_rowscale_swiglu(fused.h2g, t["Wgu"], fused.r2, out=fused.a,
+                                                                 gu=fused.gu), fl_up, up_bytes)])]
+    fused.fwd().bwd()
+    unfused.fwd_unfused()
+    nbF = G.coda_num_col_tiles(F)
+    b1_bytes = 2.0 * (M * d + F * d + 2 * M * 2 * F) + 4.0 * (M + M * nbF)
+    res_bytes = 2.0 * (M * 2 * F + d * 2 * F + 3 * M * d + d) + 4.0 * (2 * M + (M // 32) * d)
+    out.append(R.entry(
+        name, "fwd_bwd", 3 * fl_fwd, lambda: fused.fwd().bwd(), lambda: unfused.fwd_unfused().bwd_unfused(),
+        "19 fused launches vs 26 unfused",
+        kernels=[("coda_gemm_rmsnorm_bwd_res (dh2 = RMSNorm-bwd of the SwiGLU path, K = 2F)",
+                  lambda: G.coda_gemm_rmsnorm_bwd_res(fused.dgur, t["Wgu"], fused.h2, t["gamma2"], fused.r2,
+                                                      fused.s2, t["gh"]), fl_up, res_bytes),
+                 ("coda_gemm_swiglu_bwd_rowdot (SwiGLU backward with the row statistic)",
+                  lambda: G.coda_gemm_swiglu_bwd_rowdot(t["gh"], t["Wdn"], fused.gu, fused.r2), fl_up / 2,
+                  b1_bytes)]))
+    return out
+
+
+def fp8_entries(R, want):
     """FP8 (E4M3) mainloop variants: the fused kernel against the FP8 plain GEMM
     plus the same stand-alone kernels. The percentage is of the FP8 dense peak,
     taken as twice the measured BF16 peak (the nominal FP8 / BF16 ratio)."""
     import torch
+    import coda_inputs as gen
+    G, dev = R.G, R.dev
+    out = []
 
     def u8(bits):
         return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).to(dev)
@@ -674,16 +843,17 @@ def fp8_suite(G, gen, dev, report, want):
         p = gen.fp8_problem(w["M"], w["K"], w["N"], seed=0)
         X, Wt, al = u8(p["A"]), u8(p["B"]), p["sA"] * p["sB"]
         c, sn = G.coda_rope_tables(w["S"], w["head_dim"], w["theta"], device=dev)
-        out = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        o = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
         hd, rc = w["head_dim"], w["rope_cols"]
         fl = 2.0 * w["M"] * w["N"] * w["K"]
-        report(name, "fwd", fl, lambda: G.coda_gemm_rope_fp8(X, Wt, al, c, sn, hd, rc, out=out),
-               lambda: (G.coda_gemm_fp8(X, Wt, al, out=out), G.coda_unfused_rope(out, c, sn, hd, rc)), "1 vs 2",
-               peak_mult=2.0)
-        report(name, "plain_gemm", fl, lambda: G.coda_gemm_fp8(X, Wt, al, out=out),
-               lambda: G.coda_gemm_fp8(X, Wt, al, out=out), "identity epilogue, both columns the same kernel",
-               peak_mult=2.0)
-        del p, X, Wt, out
+        by = 1.0 * (w["M"] + w["N"]) * w["K"] + 2.0 * w["M"] * w["N"]
+        out.append(R.entry(name, "fwd", fl, lambda: G.coda_gemm_rope_fp8(X, Wt, al, c, sn, hd, rc, out=o),
+                           lambda: (G.coda_gemm_fp8(X, Wt, al, out=o), G.coda_unfused_rope(o, c, sn, hd, rc)),
+                           "1 vs 2", peak_mult=2.0, fused_bytes=by))
+        out.append(R.entry(name, "plain_gemm", fl, lambda: G.coda_gemm_fp8(X, Wt, al, out=o),
+                           lambda: G.coda_gemm_fp8(X, Wt, al, out=o), "identity epilogue, both columns the same kernel",
+                           peak_mult=2.0, fused_bytes=by))
+        del p, X, Wt, o
     name = "fp8_swiglu_up_4096"
     if want(name):
         w = gen.WORKLOADS[name]
@@ -693,12 +863,13 @@ def fp8_suite(G, gen, dev, report, want):
         A = torch.empty((w["M"], F), dtype=torch.bfloat16, device=dev)
         GU = torch.empty((w["M"], 2 * F), dtype=torch.bfloat16, device=dev)
         fl = 2.0 * w["M"] * w["N"] * w["K"]
-        report(name, "fwd", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A),
-               lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)), "1 vs 2 (no GU saved)",
-               peak_mult=2.0)
-        report(name, "fwd_save_gu", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A, gu=GU),
-               lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)),
-               "1 vs 2 (GU saved for backward)", peak_mult=2.0)
+        by = 1.0 * (w["M"] + w["N"]) * w["K"] + 2.0 * w["M"] * F
+        out.append(R.entry(name, "fwd", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A),
+                           lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)),
+                           "1 vs 2 (no GU saved)", peak_mult=2.0, fused_bytes=by))
+        out.append(R.entry(name, "fwd_save_gu", fl, lambda: G.coda_gemm_swiglu_fp8(X, Wt, al, out=A, gu=GU),
+                           lambda: (G.coda_gemm_fp8(X, Wt, al, out=GU), G.coda_unfused_swiglu(GU)),
+                           "1 vs 2 (GU saved for backward)", peak_mult=2.0, fused_bytes=by + 4.0 * w["M"] * F))
         del p, X, Wt, A, GU
     name = "fp8_lm_head_ce_8192"
     if want(name):
@@ -714,51 +885,69 @@ def fp8_suite(G, gen, dev, report, want):
             pm, ps, pa, tg = G.coda_gemm_ce_lse_fp8(H, Wt, al, y)
             st["lse"] = G.coda_ce_reduce(pm, ps, pa, tg)[0]
 
-        report(name, "fwd", fl, fused_ce, lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits),
-                                                   G.coda_unfused_ce_fwd(logits, y)),
-               "GEMM+partials + reduce vs GEMM (bf16 logits) + CE", peak_mult=2.0)
+        out.append(R.entry(name, "fwd", fl, fused_ce, lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits),
+                                                               G.coda_unfused_ce_fwd(logits, y)),
+                           "GEMM+partials + reduce vs GEMM (bf16 logits) + CE", peak_mult=2.0,
+                           kernels=[("coda_gemm_ce_lse_fp8", lambda: G.coda_gemm_ce_lse_fp8(H, Wt, al, y), fl,
+                                     1.0 * (w["M"] + w["N"]) * w["K"])]))
         fused_ce()
         lse = st["lse"]
-        report(name, "bwd_dlogits", fl, lambda: G.coda_gemm_ce_bwd_fp8(H, Wt, al, y, lse, 1.0 / w["M"], out=logits),
-               lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits), G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / w["M"])),
-               "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel", peak_mult=2.0)
+        out.append(R.entry(name, "bwd_dlogits", fl,
+                           lambda: G.coda_gemm_ce_bwd_fp8(H, Wt, al, y, lse, 1.0 / w["M"], out=logits),
+                           lambda: (G.coda_gemm_fp8(H, Wt, al, out=logits),
+                                    G.coda_unfused_ce_bwd(logits, y, lse, 1.0 / w["M"])),
+                           "recompute GEMM with dl epilogue vs recompute GEMM + CE-bwd kernel", peak_mult=2.0,
+                           fused_bytes=1.0 * (w["M"] + w["N"]) * w["K"] + 2.0 * w["M"] * w["N"]))
         del p, H, Wt, logits
-    torch.cuda.empty_cache()
+    return out
 
 
-def block_suite(G, gen, dev, report, dm):
-    """One period of the block-level chain (RoPE-path and SwiGLU-path
-    GEMM-residual-RMSNorm-GEMM structures) at 16K tokens, forward and forward +
-    backward, fused sequence vs unfused sequence. Inputs are drawn on the
-    device (seeded torch generator) with the distributions of
-    coda_inputs.block_problem: a host-side draw of the 70B-scale tensors would
-    take longer than the timing itself."""
+# The workloads of the default run's `configs` object (every config but the
+# headline's), and of --suite.
+CONFIG_WORKLOADS = ("rmsnorm_chain_tiny", "swiglu_up_4096", "rmsnorm_chain_8192", "lm_head_ce_8192", "block_d4096")
+SUITE_WORKLOADS = ("rmsnorm_chain_tiny", "rmsnorm_chain_8192", "rope_qkv_4096", "swiglu_up_4096",
+                   "lm_head_ce_8192", "block_d2048", "block_d4096", "block_d8192", "fp8_rope_qkv_4096",
+                   "fp8_swiglu_up_4096", "fp8_lm_head_ce_8192")
+
+
+def run_workload(R, name):
     import torch
-    c = gen.WORKLOADS[f"block_d{dm}"]
-    M, d, F, hd, rc, S = c["M"], c["d"], c["F"], c["head_dim"], c["rope_cols"], c["S"]
-    g = torch.Generator(device=dev)
-    g.manual_seed(0)
-
-    def normal(shape, std=1.0, mean=0.0):
-        t = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
-        return (t * std + mean).to(torch.bfloat16)
-
-    t = dict(P=normal((M, F)), Wd=normal((F, d), F ** -0.5), x=normal((M, d)), gamma1=normal((d,), 0.1, 1.0),
-             Wqkv=normal((d, 3 * d), d ** -0.5), O=normal((M, d)), Wo=normal((d, d), d ** -0.5),
-             gamma2=normal((d,), 0.1, 1.0), Wgu=normal((d, 2 * F), d ** -0.5), dQKV=normal((M, 3 * d)),
-             gh=normal((M, d)), Wdn=normal((F, d), F ** -0.5))
-    cos, sin = G.coda_rope_tables(S, hd, c["theta"], device=dev)
-    fl_fwd = 2.0 * M * d * (3 * F + 4 * d)
-    fused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"])
-    unfused = G.CodaBlock(t, hd, rc, cos, sin, c["eps"], unfused=True)
-    name = f"block_d{dm}"
-    report(name, "fwd", fl_fwd, fused.fwd, unfused.fwd_unfused, "6 fused launches vs 10 unfused")
-    fused.fwd()
-    unfused.fwd_unfused()
-    report(name, "fwd_bwd", 3 * fl_fwd, lambda: fused.fwd().bwd(), lambda: unfused.fwd_unfused().bwd_unfused(),
-           "19 fused launches vs 26 unfused")
-    del t, fused, unfused
+    if name == "rmsnorm_chain_tiny":
+        out = rms_chain_entries(R, name, 256, 512)
+    elif name == "rmsnorm_chain_8192":
+        out = rms_chain_entries(R, name, 8192, 8192)
+    elif name == "rope_qkv_4096":
+        out = rope_entries(R)
+    elif name == "swiglu_up_4096":
+        out = swiglu_entries(R)
+    elif name == "lm_head_ce_8192":
+        out = ce_entries(R)
+    elif name.startswith("block_d"):
+        out = block_entries(R, int(name[len("block_d"):]))
+    elif name.startswith("fp8_"):
+        out = fp8_entries(R, lambda n: n == name)
+    else:
+        raise ValueError(f"unknown workload {name}")
+    torch.cuda.synchronize(R.dev)
     torch.cuda.empty_cache()
+    return out
+
+
+def suite(a):
+    """Fused vs unfused time of every operator on every workload; one JSON line each."""
+    import torch
+    from gemm_epilogue_transformer_gb300 import build_lib
+    build_lib.build()
+    import gemm_epilogue_transformer_gb300 as G
+    G.coda_init(0)
+    R = Runner(G, torch.device("cuda", 0), a.reps)
+    for name in SUITE_WORKLOADS:
+        if a.only is None or a.only == name:
+            for e in run_workload(R, name):
+                print(json.dumps(e), flush=True)
+    status = G.coda_device_status(clear=True)
+    print(json.dumps({"suite": "done", "device_status": status}), flush=True)
+    return 0 if status == 0 else 1
 
 
 if __name__ == "__main__":
