@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--only", default=None,
                     help="with --suite: run one workload (rmsnorm_chain_tiny, rmsnorm_chain_8192, rope_qkv_4096, "
                          "swiglu_up_4096, lm_head_ce_8192, block_d2048, block_d4096, block_d8192, fp8_rope_qkv_4096, "
-                         "fp8_swiglu_up_4096, fp8_lm_head_ce_8192)")
+                         "fp8_swiglu_up_4096, fp8_lm_head_ce_8192, ce_bwd_f2_bound, gemm_vs_cublas)")
     return ap.parse_args()
 
 
@@ -902,12 +902,75 @@ def fp8_entries(R, want):
     return out
 
 
+def ce_f2_entries(R):
+    """Bound on what consuming the cross-entropy gradient on chip could save
+    (dl never stored, never re-read): the backward as built (the recompute GEMM
+    whose epilogue writes dl, then dH = dl W^T and dW = H^T dl) against the same
+    three GEMMs with the recompute GEMM storing nothing (its forward twin, which
+    keeps only per-tile statistics). The difference is the dl write plus the
+    dl-forming epilogue; a fused design would still run all three contractions."""
+    import torch
+    G, dev = R.G, R.dev
+    M, K, V = 8192, 4096, 32768
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    H, W = nrm((M, K)), nrm((K, V), K ** -0.5)
+    y = torch.randint(0, V, (M,), generator=g, device=dev, dtype=torch.int32)
+    pm, ps, pa, tg = G.coda_gemm_ce_lse(H, W, y)
+    lse = G.coda_ce_reduce(pm, ps, pa, tg)[0]
+    dl = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    dH = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((K, V), dtype=torch.bfloat16, device=dev)
+    G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=dl)
+
+    def built():
+        G.coda_gemm_ce_bwd(H, W, y, lse, 1.0 / M, out=dl)
+        G.coda_gemm(dl, W, transB=True, out=dH)
+        G.coda_gemm(H, dl, transA=True, out=dW)
+
+    def bound():
+        G.coda_gemm_ce_lse(H, W, y)
+        G.coda_gemm(dl, W, transB=True, out=dH)
+        G.coda_gemm(H, dl, transA=True, out=dW)
+
+    e = R.entry("lm_head_ce_8192", "bwd_chain_f2_bound", 3 * 2.0 * M * V * K, built, bound,
+                "fused column: dl-forming GEMM + dH + dW as built; unfused column: the same three GEMMs "
+                "with the recompute GEMM storing no dl (the most an on-chip dl could save)")
+    e["f2_max_gain"] = e["fused_ms"] / e["unfused_ms"]
+    return [e]
+
+
+def cublas_entries(R):
+    """The library's plain GEMM (identity epilogue) next to cuBLAS (torch.matmul)
+    on the same operands: the mainloop's distance from the vendor library. The
+    `unfused` column is cuBLAS here."""
+    import torch
+    G, dev = R.G, R.dev
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    nrm = _dev_normal(g, dev)
+    out = []
+    for M, N, K in ((4096, 12288, 4096), (4096, 14336, 4096), (8192, 8192, 8192), (16384, 28672, 4096)):
+        A, B = nrm((M, K)), nrm((K, N), K ** -0.5)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        C2 = torch.empty_like(C)
+        e = R.entry(f"gemm_vs_cublas_{M}x{N}x{K}", "plain_gemm", 2.0 * M * N * K,
+                    lambda: G.coda_gemm(A, B, out=C), lambda: torch.matmul(A, B, out=C2),
+                    "fused column: coda_gemm (identity epilogue); unfused column: torch.matmul (cuBLAS)",
+                    fused_bytes=2.0 * (M * K + K * N + M * N))
+        e["coda_over_cublas_throughput"] = e["unfused_ms"] / e["fused_ms"]
+        out.append(e)
+        del A, B, C, C2
+    return out
+
+
 # The workloads of the default run's `configs` object (every config but the
 # headline's), and of --suite.
 CONFIG_WORKLOADS = ("rmsnorm_chain_tiny", "swiglu_up_4096", "rmsnorm_chain_8192", "lm_head_ce_8192", "block_d4096")
 SUITE_WORKLOADS = ("rmsnorm_chain_tiny", "rmsnorm_chain_8192", "rope_qkv_4096", "swiglu_up_4096",
                    "lm_head_ce_8192", "block_d2048", "block_d4096", "block_d8192", "fp8_rope_qkv_4096",
-                   "fp8_swiglu_up_4096", "fp8_lm_head_ce_8192")
+                   "fp8_swiglu_up_4096", "fp8_lm_head_ce_8192", "ce_bwd_f2_bound", "gemm_vs_cublas")
 
 
 def run_workload(R, name):
@@ -924,6 +987,10 @@ def run_workload(R, name):
         out = ce_entries(R)
     elif name.startswith("block_d"):
         out = block_entries(R, int(name[len("block_d"):]))
+    elif name == "ce_bwd_f2_bound":
+        out = ce_f2_entries(R)
+    elif name == "gemm_vs_cublas":
+        out = cublas_entries(R)
     elif name.startswith("fp8_"):
         out = fp8_entries(R, lambda n: n == name)
     else:

@@ -35,6 +35,48 @@ __device__ __forceinline__ float exp_f(float x) { return ex2_approx(x * kLog2e);
 // 0, for g above about 88 it is 1: the correct limits.
 __device__ __forceinline__ float sigmoid_f(float g) { return rcp_approx(1.0f + exp_f(-g)); }
 
+// Two fp32 lanes per instruction (the sm_100 family's packed f32x2 forms):
+// each lane rounds exactly as the scalar multiply, add or fused multiply-add.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+// sigmoid_f on two lanes
+__device__ __forceinline__ float2 sigmoid2(float2 g) {
+  const float2 t = mul2(g, splat2(-kLog2e));
+  const float2 den = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), splat2(1.0f));
+  return make_float2(rcp_approx(den.x), rcp_approx(den.y));
+}
+// Gate and up values of features j and j+1 from their stored pair words
+// (bf16 G at the even column, the lower half of the word; U the upper half).
+__device__ __forceinline__ void gu_unpack2(uint32_t wj, uint32_t wj1, float2& G, float2& U) {
+  G = make_float2(bf16_lo(wj), bf16_lo(wj1));
+  U = make_float2(bf16_hi(wj), bf16_hi(wj1));
+}
+// SwiGLU backward of two features: with s = sigmoid(G),
+// dG = (dA s) U (1 + G (1 - s)), dU = (dA s) G.
+__device__ __forceinline__ void swiglu_bwd2(float2 dA, float2 G, float2 U, float2& dG, float2& dU) {
+  const float2 s = sigmoid2(G);
+  const float2 as = mul2(dA, s);
+  dU = mul2(as, G);
+  const float2 q = fma2(G, fma2(s, splat2(-1.0f), splat2(1.0f)), splat2(1.0f));
+  dG = mul2(mul2(as, U), q);
+}
+// Write 16 packed words (32 bf16) as one 64-byte staging row.
+__device__ __forceinline__ void stage_words16(uint32_t box, int r, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) stage_put(box, r, q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+__device__ __forceinline__ void words16(const uint4 (&u)[4], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    w[4 * q] = u[q].x;
+    w[4 * q + 1] = u[q].y;
+    w[4 * q + 2] = u[q].z;
+    w[4 * q + 3] = u[q].w;
+  }
+}
+
 // Shared-memory trade: an epilogue may declare kStageBufs = 1 (single-buffered
 // store staging), kInRingBytes = 4096 (a smaller input ring) or kMaxSlots = 1
 // (one store box per chunk). Each frees room for a sixth mainloop stage on SM
@@ -283,21 +325,20 @@ struct EpiSwiGLUBwd {
                                uint32_t in, uint32_t box0, uint32_t box1) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      float g[32];
       uint4 u[4];
       box_row(in + half * kInBoxBytes, cx.lane, u);
-      unpack32(u, g);
-      float o[32];
+      uint32_t w[16];
+      words16(u, w);
+      // features j, j+1 as two-lane vectors; each (dG, dU) pair packs into one word
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        // dG = dA U s (1 + G (1 - s)), dU = dA G s, sharing dA s
-        const float G = g[2 * k], U = g[2 * k + 1];
-        const float s = sigmoid_f(G);
-        const float as = acc[16 * half + k] * s;
-        o[2 * k] = (as * U) * fmaf(G, 1.0f - s, 1.0f);
-        o[2 * k + 1] = as * G;
+      for (int j = 0; j < 16; j += 2) {
+        float2 G, U, dG, dU;
+        gu_unpack2(w[j], w[j + 1], G, U);
+        swiglu_bwd2(make_float2(acc[16 * half + j], acc[16 * half + j + 1]), G, U, dG, dU);
+        w[j] = pack_bf16(dG.x, dU.x);
+        w[j + 1] = pack_bf16(dG.y, dU.y);
       }
-      stage_row32(half ? box1 : box0, cx.lane, o);
+      stage_words16(half ? box1 : box0, cx.lane, w);
     }
   }
   __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
@@ -672,7 +713,8 @@ struct EpiSwiGLUBwdRowdot {
     float* pdot;              // [M, ceil(F/128)]
   };
   struct State {
-    float dot, rv;
+    float2 dot;  // even and odd features' shares of the row dot
+    float rv;
   };
   CODA_NO_PREFETCH
   static constexpr int kInBoxes = 2;
@@ -688,33 +730,31 @@ struct EpiSwiGLUBwdRowdot {
   static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    st.dot = 0.f;
+    st.dot = splat2(0.f);
     st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
                                uint32_t in, uint32_t box0, uint32_t box1) {
+    const float2 rv = splat2(st.rv);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      float g[32];
       uint4 u[4];
       box_row(in + half * kInBoxBytes, cx.lane, u);
-      unpack32(u, g);
-      float o[32];
+      uint32_t w[16];
+      words16(u, w);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        // o = r (dG, dU) with dG = dA U s (1 + G (1 - s)), dU = dA G s; the row
-        // dot accumulates on the scaled values and end() divides r out once
-        const float G = g[2 * k], U = g[2 * k + 1];
-        const float sg = sigmoid_f(G);
-        const float as = (acc[16 * half + k] * st.rv) * sg;
-        const float rdG = (as * U) * fmaf(G, 1.0f - sg, 1.0f);
-        const float rdU = as * G;
-        st.dot = fmaf(rdG, G, st.dot);
-        st.dot = fmaf(rdU, U, st.dot);
-        o[2 * k] = rdG;
-        o[2 * k + 1] = rdU;
+      for (int j = 0; j < 16; j += 2) {
+        // r (dG, dU) from r dA; the row dot accumulates on the scaled values
+        // and end() divides r out once
+        float2 G, U, rdG, rdU;
+        gu_unpack2(w[j], w[j + 1], G, U);
+        swiglu_bwd2(mul2(make_float2(acc[16 * half + j], acc[16 * half + j + 1]), rv), G, U, rdG, rdU);
+        st.dot = fma2(rdG, G, st.dot);
+        st.dot = fma2(rdU, U, st.dot);
+        w[j] = pack_bf16(rdG.x, rdU.x);
+        w[j + 1] = pack_bf16(rdG.y, rdU.y);
       }
-      stage_row32(half ? box1 : box0, cx.lane, o);
+      stage_words16(half ? box1 : box0, cx.lane, w);
     }
   }
   __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
@@ -724,7 +764,7 @@ struct EpiSwiGLUBwdRowdot {
   }
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
     // r > 0 for every row inside M (r = 1 / sqrt(mean + eps))
-    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot / st.rv;
+    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = (st.dot.x + st.dot.y) / st.rv;
   }
 };
 

@@ -130,6 +130,11 @@ using CfgOf = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value, Stag
 
 constexpr int BSEG = 128;  // epilogue segment: columns per partial-statistics block
 
+// L2 cache policy of the epilogue's input boxes and stores: they stream
+// through once, and evict-first keeps them from displacing operand tiles that
+// later tiles read again.
+constexpr bool kEpiEvictFirst = true;
+
 struct GemmShape {
   int M, N, K;
   int a_mn, b_mn;  // 0: K-major; 1: MN-major, 64-wide 2-D boxes; 2: MN-major, one 3-D box per stage
@@ -545,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so load latency overlaps TMEM reads, math and the mainloop.
     const int ew = warp & 3;
     const uint32_t my_stage = smem_u32(s_epi) + ew * C::kEpiWarpBytes;
+    const uint64_t pol_stream = kEpiEvictFirst ? l2_policy_evict_first() : 0ull;
+    (void)pol_stream;
     if constexpr (C::kSharedBytes > 0) {
       // the 128 epilogue threads fill the table together, then wait for each other
       Epi::init_shared(ep, smem_u32(s_tab), static_cast<int>(threadIdx.x) - 64);
@@ -595,7 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < kIn; ++b) {
               int map, x, y;
               Epi::in_coord(ep, ic, it_c, b, map, x, y);
-              tma_load_2d(dst + b * kInBoxBytes, map ? &tmI1 : &tmI0, bar, x, y);
+              if constexpr (kEpiEvictFirst)
+                tma_load_2d_hint(dst + b * kInBoxBytes, map ? &tmI1 : &tmI0, bar, x, y, pol_stream);
+              else
+                tma_load_2d(dst + b * kInBoxBytes, map ? &tmI1 : &tmI0, bar, x, y);
             }
             ++seq_issued;
           }
@@ -671,7 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int s = 0; s < nslots; ++s) {
                 int map, x, y;
                 Epi::store_coord(ep, cx, cs, s, map, x, y);
-                tma_store_2d(map ? &tmO1 : &tmO0, box0 + s * kStageBoxBytes, x, y);
+                if constexpr (kEpiEvictFirst)
+                  tma_store_2d_hint(map ? &tmO1 : &tmO0, box0 + s * kStageBoxBytes, x, y, pol_stream);
+                else
+                  tma_store_2d(map ? &tmO1 : &tmO0, box0 + s * kStageBoxBytes, x, y);
               }
               bulk_commit();
             }
