@@ -150,8 +150,10 @@ int check_block(const char* fn, const coda_block_t* b) {
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB: M * ceil(d/128) fp32 partials
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device (with that device current) and cached; nullptr after fail().
+// Device address of g_noalloc_scratch on the current device, looked up by the
+// first call on each device (with that device current) and cached for the
+// process, which assumes one context per device (as every per-device cache of
+// the library does); nullptr after fail().
 void* noalloc_scratch() {
   static std::mutex mu;
   static void* ptrs[64] = {nullptr};

@@ -40,6 +40,11 @@
  *     that runs out sets CODA_DEVST_TIMEOUT in the device status word and the
  *     kernel returns early. Out-of-range labels set CODA_DEVST_BAD_LABEL.
  *     Read (and clear) the word with coda_device_status().
+ *   - Per-device state (the status word's address, kernel attributes, the
+ *     cluster count, the no-allocation scratch's address) is set up by the
+ *     first call on a device and kept for the life of the process: it assumes
+ *     one CUDA context per device. After cudaDeviceReset() on a device, do not
+ *     use the library on that device again in the same process.
  */
 #ifndef CODA_H_
 #define CODA_H_
@@ -459,7 +464,10 @@ int coda_block_fwd(const coda_block_t* b, coda_stream_t stream);
  * CODA_ERR_UNSUPPORTED (M = 16384 fits up to d = 8192). Two calls whose
  * kernels can overlap on the GPU (calls on different streams, or from threads
  * whose streams are not ordered) race on that array and give undefined
- * results; calls on one stream run in order and are safe. Allocates nothing. */
+ * results; calls on one stream run in order and are safe. Allocates nothing.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and keeps it for the process; make
+ * that first call before any stream capture. */
 int coda_block_fwd_noalloc(const coda_block_t* b, coda_stream_t stream);
 
 /* Fused backward (after coda_block_fwd on the same descriptor):
