@@ -677,17 +677,26 @@ struct EpiRmsNormBwd {
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
                                uint32_t in, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
-    float h[32], g[32], part[32];
+    float part[32];
     uint4 u[4];
     box_row(in, cx.lane, u);
-    unpack32(u, h);
-    unpack32(pr.g, g);
+    uint32_t hw[16], gw[16], w[16];
+    words16(u, hw);
+    words16(pr.g, gw);
+    const float2 rv = splat2(st.rv), nr2s = splat2(-st.r2s);
+    // columns 2j, 2j+1 as two-lane vectors: rG = r G; partial r G h; dh1 = gamma rG - r^2 s h1
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      part[i] = st.rv * acc[i] * h[i];
-      acc[i] = st.rv * g[i] * acc[i] - st.r2s * h[i];
+    for (int j = 0; j < 16; ++j) {
+      const float2 h = make_float2(bf16_lo(hw[j]), bf16_hi(hw[j]));
+      const float2 g = make_float2(bf16_lo(gw[j]), bf16_hi(gw[j]));
+      const float2 rG = mul2(make_float2(acc[2 * j], acc[2 * j + 1]), rv);
+      const float2 pt = mul2(rG, h);
+      part[2 * j] = pt.x;
+      part[2 * j + 1] = pt.y;
+      const float2 o = fma2(g, rG, mul2(nr2s, h));
+      w[j] = pack_bf16(o.x, o.y);
     }
-    stage_row32(box0, cx.lane, acc);
+    stage_words16(box0, cx.lane, w);
     const float tot = warp_colsum32(part, cx.lane);
     // rows past M contribute zeros; a warp slice that starts past M has no partial row
     if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
@@ -814,21 +823,29 @@ struct EpiRmsNormBwdRes {
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
                                uint32_t in, uint32_t box0, uint32_t) {
     const int col0 = cx.n0 + 32 * c;
-    float h[32], g[32], part[32];
-    uint4 u[4];
+    float part[32];
+    uint4 u[4], v[4];
     box_row(in, cx.lane, u);
-    unpack32(u, h);
-    unpack32(pr.g, g);
+    box_row(in + kInBoxBytes, cx.lane, v);
+    uint32_t hw[16], dw[16], gw[16], w[16];
+    words16(u, hw);
+    words16(v, dw);
+    words16(pr.g, gw);
+    const float2 nr2s = splat2(-st.r2s);
+    // columns 2j, 2j+1 as two-lane vectors: partial Gr h; dh = gamma Gr - r^2 s h + dres
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      part[i] = acc[i] * h[i];
-      acc[i] = g[i] * acc[i] - st.r2s * h[i];
+    for (int j = 0; j < 16; ++j) {
+      const float2 h = make_float2(bf16_lo(hw[j]), bf16_hi(hw[j]));
+      const float2 g = make_float2(bf16_lo(gw[j]), bf16_hi(gw[j]));
+      const float2 dres = make_float2(bf16_lo(dw[j]), bf16_hi(dw[j]));
+      const float2 Gr = make_float2(acc[2 * j], acc[2 * j + 1]);
+      const float2 pt = mul2(Gr, h);
+      part[2 * j] = pt.x;
+      part[2 * j + 1] = pt.y;
+      const float2 o = add2(fma2(g, Gr, mul2(nr2s, h)), dres);
+      w[j] = pack_bf16(o.x, o.y);
     }
-    box_row(in + kInBoxBytes, cx.lane, u);
-    unpack32(u, h);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] += h[i];
-    stage_row32(box0, cx.lane, acc);
+    stage_words16(box0, cx.lane, w);
     const float tot = warp_colsum32(part, cx.lane);
     if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
       ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
