@@ -52,7 +52,9 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="time every fused operator against its unfused pair on all five workloads "
                          "(one JSON line per operator) instead of the headline step")
-    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite")
+    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite (at least)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="with --suite: raise each entry's repetitions until its timed region lasts this long")
     ap.add_argument("--only", default=None,
                     help="with --suite: run one workload (rmsnorm_chain_tiny, rmsnorm_chain_8192, rope_qkv_4096, "
                          "swiglu_up_4096, lm_head_ce_8192, block_d2048, block_d4096, block_d8192, fp8_rope_qkv_4096, "
@@ -1007,7 +1009,7 @@ def suite(a):
     build_lib.build()
     import gemm_epilogue_transformer_gb300 as G
     G.coda_init(0)
-    R = Runner(G, torch.device("cuda", 0), a.reps)
+    R = Runner(G, torch.device("cuda", 0), a.reps, min_s=a.min_seconds)
     for name in SUITE_WORKLOADS:
         if a.only is None or a.only == name:
             for e in run_workload(R, name):
