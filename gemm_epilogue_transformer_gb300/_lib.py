@@ -7,7 +7,9 @@ import ctypes
 import os
 from ctypes import POINTER, Structure, c_char_p, c_double, c_float, c_int, c_size_t, c_uint64, c_void_p
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
+# CODA_LIBRARY names another build of the same library to load instead (the
+# checked build, libcoda_checked.so, next to this file).
+LIB_PATH = os.environ.get("CODA_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoda.so")
 
 P = c_void_p  # any device pointer (bf16 / fp32 / int32) or stream handle
 I = c_int
@@ -98,8 +100,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         return _lib
     if not os.path.exists(path):
         raise RuntimeError(
-            f"libcoda.so not found at {path}: build it with "
-            "`python -m gemm_epilogue_transformer_gb300.build_lib` (needs nvcc for sm_103a)")
+            f"{os.path.basename(path)} not found at {path}: build it with "
+            "`python -m gemm_epilogue_transformer_gb300.build_lib` (add --checked for the checked build; "
+            "needs nvcc for sm_103a)")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         f = getattr(lib, name)

@@ -1,7 +1,10 @@
 """Build libcoda.so in-tree: one nvcc per translation unit in parallel, for
 sm_103a only, then a shared-library link with the static CUDA runtime.
+``--checked`` builds the same sources with CODA_CHECKED=1 into
+libcoda_checked.so: every direct global access of the fused epilogues tests
+its index against the tensor's extent first (CODA_DEVST_BOUNDS on a miss).
 
-Usage: ``python -m gemm_epilogue_transformer_gb300.build_lib [--force] [-v]``
+Usage: ``python -m gemm_epilogue_transformer_gb300.build_lib [--force] [--checked] [-v]``
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcoda.so")
+LIB_CHECKED = os.path.join(PKG, "libcoda_checked.so")
 
 SOURCES = ["runtime.cu", "aux.cu", "unfused.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_chain.cu", "block.cu",
            "gemm_fp8.cu"]
@@ -38,27 +42,32 @@ def _deps():
     return out
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile every translation unit for sm_103a and link libcoda.so; return its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, checked: bool = False) -> str:
+    """Compile every translation unit for sm_103a and link libcoda.so (or, with
+    checked, libcoda_checked.so); return its path."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
+    bdir = os.path.join(BUILD, "checked") if checked else BUILD
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     flags = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-I", INCLUDE,
              "--expt-relaxed-constexpr", "-diag-suppress", "177"]
+    if checked:
+        flags += ["-DCODA_CHECKED=1"]
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -73,15 +82,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, "-shared", *ARCH, "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode:
         raise RuntimeError(f"link failed:\n{r.stdout}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):
@@ -89,8 +98,9 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
     ap.add_argument("--ptxas-verbose", action="store_true")
+    ap.add_argument("--checked", action="store_true", help="build libcoda_checked.so (bounds-tested epilogues)")
     a = ap.parse_args(argv)
-    print(build(force=a.force, verbose=a.verbose, ptxas_verbose=a.ptxas_verbose))
+    print(build(force=a.force, verbose=a.verbose, ptxas_verbose=a.ptxas_verbose, checked=a.checked))
 
 
 if __name__ == "__main__":

@@ -204,7 +204,8 @@ struct EpiResRmsPrep {
   }
   CODA_STORE_SAME_COLS(1)
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) ep.psq[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.sumsq;
+    const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+    if (cx.row < cx.M && CODA_IN(cx, i, static_cast<long>(cx.M) * cx.n_blocks)) ep.psq[i] = st.sumsq;
   }
 };
 
@@ -223,7 +224,7 @@ struct EpiRowScale {
   static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+    st.rv = (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
                                uint32_t, uint32_t box0, uint32_t) {
@@ -262,7 +263,7 @@ struct EpiSwiGLU {
   // slot 0: A (32 outputs from two chunks); slots 1, 2: GU of the two chunks
   __device__ static int slots(const Params&) { return kSaveGU ? 3 : 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+    if constexpr (kScale) st.rv = (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
                                uint32_t, uint32_t box0, uint32_t) {
@@ -392,14 +393,16 @@ struct EpiRope {
   __device__ static uint32_t lane_addr(uint32_t base, int t, int l, int j) {
     return base + t * (32 * 256) + l * 256 + ((j ^ (l & 7)) << 4);
   }
-  __device__ static void init_shared(const Params& ep, uint32_t base, int tid) {
+  __device__ static void init_shared(const Params& ep, uint32_t base, int tid, int* status) {
     if (!ep.lane_tables) return;
     const int g = ep.head_dim >> 3;  // 16-byte granules per table row (head_dim / 2 floats)
+    const long extent = static_cast<long>(ep.S) * (ep.head_dim >> 1);
     for (int idx = tid; idx < 2 * 32 * g; idx += 128) {
       const int t = idx / (32 * g), rem = idx - t * 32 * g;
       const int l = rem / g, j = rem - l * g;
-      const float* src = (t ? ep.sin_tab : ep.cos_tab) + static_cast<long>(l) * (ep.head_dim >> 1) + 4 * j;
-      const uint4 v = ldg_nc_v4(src);
+      const long off = static_cast<long>(l) * (ep.head_dim >> 1) + 4 * j;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (CODA_IN_ST(status, off + 3, extent)) v = ldg_nc_v4((t ? ep.sin_tab : ep.cos_tab) + off);
       st_shared_v4(lane_addr(base, t, l, j), v.x, v.y, v.z, v.w);
     }
   }
@@ -409,12 +412,14 @@ struct EpiRope {
       const int pos = ep.lane_tables ? (cx.wrow0 % ep.S) : ((cx.row < cx.M) ? (cx.row % ep.S) : 0);
       const int half = ep.head_dim >> 1;
       const int i0 = (col0 % ep.head_dim) >> 1;
-      const float* cp = ep.cos_tab + static_cast<long>(pos) * half + i0;
-      const float* sp = ep.sin_tab + static_cast<long>(pos) * half + i0;
+      const long off = static_cast<long>(pos) * half + i0;
+      const float* cp = ep.cos_tab + off;
+      const float* sp = ep.sin_tab + off;
+      const bool in = CODA_IN(cx, off + 15, static_cast<long>(ep.S) * half);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        pr.c[q] = ldg_nc_v4(cp + 4 * q);
-        pr.s[q] = ldg_nc_v4(sp + 4 * q);
+        pr.c[q] = in ? ldg_nc_v4(cp + 4 * q) : make_uint4(0, 0, 0, 0);
+        pr.s[q] = in ? ldg_nc_v4(sp + 4 * q) : make_uint4(0, 0, 0, 0);
       }
     }
   }
@@ -422,7 +427,7 @@ struct EpiRope {
   static constexpr int kMaxSlots = 1;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    if constexpr (kScale) st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+    if constexpr (kScale) st.rv = (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre& pr,
                                uint32_t, uint32_t box0, uint32_t) {
@@ -505,7 +510,7 @@ struct EpiCeLse {
     st.s = 0.f;
     st.best = -1;
     st.label = -1;
-    if (cx.row < cx.M) {
+    if (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) {
       st.label = ep.labels[cx.row];
       if (cx.n_blk == 0 && (st.label < 0 || st.label >= cx.N)) {
         atomicOr(ep.status, CODA_DEVST_BAD_LABEL);
@@ -536,7 +541,7 @@ struct EpiCeLse {
       st.m = nm;
     }
     const int rel = st.label - col0;
-    if (rel >= 0 && rel < 32 && cx.row < cx.M) {
+    if (rel >= 0 && rel < 32 && cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) {
       float t = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -550,8 +555,8 @@ struct EpiCeLse {
     y = 0;
   }
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) {
-      const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+    const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+    if (cx.row < cx.M && CODA_IN(cx, i, static_cast<long>(cx.M) * cx.n_blocks)) {
       ep.pmax[i] = st.m;
       ep.psum[i] = st.s;
       if (ep.parg) ep.parg[i] = st.best;
@@ -577,8 +582,9 @@ struct EpiCeBwd {
   static constexpr int kMaxSlots = 2;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    st.label = (cx.row < cx.M) ? ep.labels[cx.row] : -1;
-    st.lse = (cx.row < cx.M) ? ep.lse[cx.row] : 0.f;
+    const bool in = cx.row < cx.M && CODA_IN(cx, cx.row, cx.M);
+    st.label = in ? ep.labels[cx.row] : -1;
+    st.lse = in ? ep.lse[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int c, float (&acc)[32], const Pre&,
                                uint32_t, uint32_t box0, uint32_t) {
@@ -617,7 +623,7 @@ struct EpiRowdot {
   __device__ static int slots(const Params& ep) { return ep.store_dyr ? 2 : 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = 0.f;
-    st.rv = (ep.store_dyr && cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+    st.rv = (ep.store_dyr && cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params& ep, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
                                uint32_t in, uint32_t box0, uint32_t box1) {
@@ -636,7 +642,8 @@ struct EpiRowdot {
   }
   CODA_STORE_SAME_COLS(1)
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = st.dot;
+    const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+    if (cx.row < cx.M && CODA_IN(cx, i, static_cast<long>(cx.M) * cx.n_blocks)) ep.pdot[i] = st.dot;
   }
 };
 
@@ -666,7 +673,7 @@ struct EpiRmsNormBwd {
   static constexpr int kInRingBytes = 4096;
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) {
+    if (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) {
       st.rv = ep.r[cx.row];
       st.r2s = st.rv * st.rv * ep.s[cx.row];
     } else {
@@ -699,8 +706,9 @@ struct EpiRmsNormBwd {
     stage_words16(box0, cx.lane, w);
     const float tot = warp_colsum32(part, cx.lane);
     // rows past M contribute zeros; a warp slice that starts past M has no partial row
-    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
-      ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
+    const long ig = static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane;
+    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N && CODA_IN(cx, ig, static_cast<long>((cx.M + 31) >> 5) * cx.N))
+      ep.pdg[ig] = tot;
   }
   CODA_STORE_SAME_COLS(0)
   __device__ static void end(State&, const Params&, const EpiCtx&) {}
@@ -740,7 +748,7 @@ struct EpiSwiGLUBwdRowdot {
   __device__ static int slots(const Params&) { return 2; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = splat2(0.f);
-    st.rv = (cx.row < cx.M) ? ep.r[cx.row] : 0.f;
+    st.rv = (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
                                uint32_t in, uint32_t box0, uint32_t box1) {
@@ -773,7 +781,9 @@ struct EpiSwiGLUBwdRowdot {
   }
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {
     // r > 0 for every row inside M (r = 1 / sqrt(mean + eps))
-    if (cx.row < cx.M) ep.pdot[static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk] = (st.dot.x + st.dot.y) / st.rv;
+    const long i = static_cast<long>(cx.row) * cx.n_blocks + cx.n_blk;
+    if (cx.row < cx.M && CODA_IN(cx, i, static_cast<long>(cx.M) * cx.n_blocks))
+      ep.pdot[i] = (st.dot.x + st.dot.y) / st.rv;
   }
 };
 
@@ -813,7 +823,7 @@ struct EpiRmsNormBwdRes {
   static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
   __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
-    if (cx.row < cx.M) {
+    if (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) {
       const float rv = ep.r[cx.row];
       st.r2s = rv * rv * ep.s[cx.row];
     } else {
@@ -847,8 +857,9 @@ struct EpiRmsNormBwdRes {
     }
     stage_words16(box0, cx.lane, w);
     const float tot = warp_colsum32(part, cx.lane);
-    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N)
-      ep.pdg[static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane] = tot;
+    const long ig = static_cast<long>(cx.wrow0 >> 5) * cx.N + col0 + cx.lane;
+    if (cx.wrow0 < cx.M && col0 + cx.lane < cx.N && CODA_IN(cx, ig, static_cast<long>((cx.M + 31) >> 5) * cx.N))
+      ep.pdg[ig] = tot;
   }
   CODA_STORE_SAME_COLS(0)
   __device__ static void end(State&, const Params&, const EpiCtx&) {}

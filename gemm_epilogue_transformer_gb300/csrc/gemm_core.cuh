@@ -151,6 +151,7 @@ struct GemmShape {
 };
 
 struct EpiCtx {
+  int* status;  // device status word (CODA_DEVST_* bits)
   int M, N;
   int m0, n0;   // this segment's first row (of the CTA's 128) and first column
   int m_blk;
@@ -163,6 +164,22 @@ struct EpiCtx {
   int k_blocks;
   uint32_t shared;  // shared-memory address of the epilogue's table (kSharedBytes), 0 if none
 };
+
+// Checked build (CODA_CHECKED=1): every direct global access of an epilogue
+// first tests its index against the extent of the tensor it touches; an index
+// outside sets CODA_DEVST_BOUNDS in the device status word and the access is
+// skipped. In the normal build the test compiles away.
+#if defined(CODA_CHECKED) && CODA_CHECKED
+__device__ __forceinline__ bool coda_in_extent(long idx, long extent, int* status) {
+  if (idx >= 0 && idx < extent) return true;
+  atomicOr(status, CODA_DEVST_BOUNDS);
+  return false;
+}
+#define CODA_IN_ST(status, idx, extent) coda_in_extent(static_cast<long>(idx), static_cast<long>(extent), (status))
+#else
+#define CODA_IN_ST(status, idx, extent) true
+#endif
+#define CODA_IN(cx, idx, extent) CODA_IN_ST((cx).status, idx, extent)
 
 // Tile order: groups of group_m row-blocks sweep all column blocks, so the
 // A rows of a group and the B columns in flight stay L2 resident.
@@ -554,13 +571,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     (void)pol_stream;
     if constexpr (C::kSharedBytes > 0) {
       // the 128 epilogue threads fill the table together, then wait for each other
-      Epi::init_shared(ep, smem_u32(s_tab), static_cast<int>(threadIdx.x) - 64);
+      Epi::init_shared(ep, smem_u32(s_tab), static_cast<int>(threadIdx.x) - 64, p.status);
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
     // Segment `seg` (128 columns) of work item tt; false if it lies past N.
     auto make_ctx = [&](int tt, int seg, EpiCtx& cx) {
       int n0, ncols;
       item_coords(tt, p, cx.m_blk, n0, ncols);
+      cx.status = p.status;
       cx.M = p.M;
       cx.N = p.N;
       cx.m0 = cx.m_blk * C::kTileM + static_cast<int>(q) * BM;

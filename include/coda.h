@@ -40,6 +40,12 @@
  *     that runs out sets CODA_DEVST_TIMEOUT in the device status word and the
  *     kernel returns early. Out-of-range labels set CODA_DEVST_BAD_LABEL.
  *     Read (and clear) the word with coda_device_status().
+ *   - A checked build of the same library (libcoda_checked.so, compiled with
+ *     CODA_CHECKED=1) tests the index of every direct global load and store
+ *     of the fused epilogues (row statistics, tile partials, per-row vectors,
+ *     RoPE tables) against the tensor's extent before the access; an index
+ *     outside sets CODA_DEVST_BOUNDS and the access is skipped. TMA loads and
+ *     stores are bounded by their tensor maps in both builds.
  *   - Per-device state (the status word's address, kernel attributes, the
  *     cluster count, the no-allocation scratch's address) is set up by the
  *     first call on a device and kept for the life of the process: it assumes
@@ -64,6 +70,7 @@ extern "C" {
 
 #define CODA_DEVST_TIMEOUT 1   /* a bounded in-kernel wait ran out            */
 #define CODA_DEVST_BAD_LABEL 2 /* a cross-entropy label was outside [0, V)    */
+#define CODA_DEVST_BOUNDS 4    /* checked build only: an epilogue's direct global access fell outside its tensor */
 
 typedef uint16_t coda_bf16;
 typedef void* coda_stream_t;

@@ -23,6 +23,16 @@ def coda():
     from gemm_epilogue_transformer_gb300 import build_lib
     build_lib.build()
     import gemm_epilogue_transformer_gb300 as G
+    if os.environ.get("CODA_LIBRARY"):
+        # a run on the checked build: any read of the status word that shows
+        # CODA_DEVST_BOUNDS fails at once, even in a test that clears the word
+        read = G.coda_device_status
+
+        def checked_status(clear=True):
+            st = read(clear)
+            assert st < 0 or not st & 4, f"checked build: an epilogue access fell outside its tensor (status {st})"
+            return st
+        G.coda_device_status = checked_status
     G.coda_init(0)
     G.coda_device_status(clear=True)
     yield G

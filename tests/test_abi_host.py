@@ -34,6 +34,15 @@ def test_header_declares_the_boundary():
     assert len(names) == len(set(names))
 
 
+def test_checked_build_exports_the_same_symbols():
+    """libcoda_checked.so (bounds-tested epilogues) is the same boundary."""
+    from gemm_epilogue_transformer_gb300 import build_lib
+    path = build_lib.build(checked=True)
+    chk = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(chk, n), f"{n} not exported by the checked build"
+
+
 def test_every_declared_symbol_is_exported_and_bound(lib):
     from gemm_epilogue_transformer_gb300 import _lib
     names = declared_functions()
