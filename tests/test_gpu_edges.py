@@ -225,3 +225,56 @@ def test_rope_last_positions(coda):
     rg = O.gemm_rope_bwd(O.bf16(p["A"]), O.bf16(p["B"]), pos, hd, theta, rc)
     assert_bf16(f64(g), rg, "rope bwd")
     assert_bf16(f64(g)[last], rg[last], "rope bwd at positions S-32..S-1")
+
+
+# ---------------------------------------------------------------- FP8 mainloop
+
+def _dev_u8(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).cuda()
+
+
+def test_ce_fp8_wide_logits(coda):
+    """The FP8 (E4M3) mainloop feeds the same online log-sum-exp: logits of
+    about +-60 formed as alpha * (H W^T) with alpha = 4 and E4M3 operands."""
+    import torch
+    M, K, V = 320, 64, 1000
+    Hb, Wb, rl = _ce_edge_problem(M, K, V)
+    # the bf16 construction re-encoded: H / 4 (40 and 60 become 10 and 15, exact in E4M3), W^T stored [V, K]
+    H8 = gen.f32_to_e4m3_bits(O.bf16(Hb).astype(np.float32) / 4.0)
+    W8 = gen.f32_to_e4m3_bits(np.ascontiguousarray(O.bf16(Wb).T.astype(np.float32)))
+    a, b, alpha = O.e4m3(H8), O.e4m3(W8), 4.0
+    L = alpha * O.matmul(a, b.T)
+    assert L.max() > 55 and L.min() < -55
+    am_ref = np.argmax(L, axis=1)
+    choice = np.stack([np.zeros(M, np.int64), np.full(M, V - 1), np.full(M, 896), am_ref, rl.integers(0, V, M)],
+                      axis=1)
+    labels = choice[np.arange(M), np.arange(M) % 5].astype(np.int32)
+    y = torch.from_numpy(labels).cuda()
+    pmax, psum, parg, tgt = coda.coda_gemm_ce_lse_fp8(_dev_u8(H8), _dev_u8(W8), alpha, y)
+    lse, loss_row, _, argmax = coda.coda_ce_reduce(pmax, psum, parg, tgt)
+    ref = O.ce_fwd(L, labels)
+    assert_stat(f64(lse), ref["lse"], "fp8 lse")
+    assert_stat(f64(loss_row), ref["loss_row"], "fp8 loss rows")
+    top2 = np.sort(L, axis=1)[:, -2:]
+    sure = (top2[:, 1] - top2[:, 0]) > 1e-5 * np.sqrt(K) * np.max(np.abs(L), axis=1) + 1e-6
+    assert sure.mean() > 0.9
+    assert np.array_equal(argmax.cpu().numpy()[sure], ref["argmax"][sure])
+    dl = coda.coda_gemm_ce_bwd_fp8(_dev_u8(H8), _dev_u8(W8), alpha, y, lse, 1.0 / M)
+    assert_bf16(f64(dl), O.ce_bwd(L, labels, f64(lse), 1.0 / M), "fp8 dl")
+
+
+def test_swiglu_fp8_saturated_gates(coda):
+    """FP8 SwiGLU forward with gates |G| up to about 200 (E4M3 operands)."""
+    M, K, F = 300, 64, 264
+    Xb, Wb, _, _ = _saturated_swiglu(M, K, F, seed=17)
+    X8 = gen.f32_to_e4m3_bits(O.bf16(Xb).astype(np.float32))
+    W8 = gen.f32_to_e4m3_bits(np.ascontiguousarray(O.bf16(Wb).T.astype(np.float32) * 8.0))  # [2F, K]
+    a, b, alpha = O.e4m3(X8), O.e4m3(W8), 0.125
+    A, GU = coda.coda_gemm_swiglu_fp8(_dev_u8(X8), _dev_u8(W8), alpha, want_gu=True)
+    ref = O.gemm_swiglu(a, alpha * b.T)
+    G = ref["GU"][:, 0::2]
+    assert np.sum(G > 88) > 100 and np.sum(G < -88) > 100
+    assert_bf16(f64(GU), ref["GU"], "fp8 GU")
+    assert_bf16(f64(A), ref["A"], "fp8 A = silu(G) U")
+    assert np.all(f64(A)[f64(GU)[:, 0::2] < -100] == 0.0)
