@@ -299,7 +299,9 @@ struct EpiSwiGLU {
 
 // ---------------------------------------------------------------- SwiGLU bwd
 // acc = dA[:, f0..f0+31]; loads the saved GU pairs, recomputes sigmoid(G), and
-// emits interleaved (dG, dU) for 64 output columns: two store boxes.
+// emits interleaved (dG, dU) for 64 output columns. The chunk's 64 GU columns
+// arrive as one 32 x 128-byte box and its 64 outputs leave as one, with the
+// 128-byte swizzle: half the TMA requests of two 64-byte boxes.
 // (pith page, Figure 7: one incoming gradient -> both paired input gradients.)
 template <int kRing = 4096>
 struct EpiSwiGLUBwd {
@@ -308,28 +310,34 @@ struct EpiSwiGLUBwd {
   };
   struct State {};
   CODA_NO_PREFETCH
-  // the 64 interleaved GU columns of the chunk's 32 gate/up pairs: two boxes
-  static constexpr int kInBoxes = 2;
+  static constexpr int kInBoxes = 2;  // ring bytes per chunk: two 64-byte boxes' worth
+  static constexpr int kInLoads = 1;  // filled by one 128-byte box
   __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }
-  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
     map = 0;
-    x = 2 * (cx.n0 + 32 * c) + 32 * b;
+    x = 2 * (cx.n0 + 32 * c);
     y = cx.wrow0;
   }
   static constexpr int kChunksPerStore = 1;
-  static constexpr int kMaxSlots = 2;
+  static constexpr int kMaxSlots = 2;  // staging bytes of two 64-byte boxes, stored as one 128-byte box
   static constexpr int kStageBufs = 1;
   static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
-  __device__ static int slots(const Params&) { return 2; }
+  __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State&, const Params&, const EpiCtx&) {}
   __device__ static void chunk(State&, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
-                               uint32_t in, uint32_t box0, uint32_t box1) {
+                               uint32_t in, uint32_t box0, uint32_t) {
+    uint4 u[8];
+    box128_row(in, cx.lane, u);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      uint4 u[4];
-      box_row(in + half * kInBoxBytes, cx.lane, u);
       uint32_t w[16];
-      words16(u, w);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        w[4 * q] = u[4 * half + q].x;
+        w[4 * q + 1] = u[4 * half + q].y;
+        w[4 * q + 2] = u[4 * half + q].z;
+        w[4 * q + 3] = u[4 * half + q].w;
+      }
       // features j, j+1 as two-lane vectors; each (dG, dU) pair packs into one word
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
@@ -339,12 +347,14 @@ struct EpiSwiGLUBwd {
         w[j] = pack_bf16(dG.x, dU.x);
         w[j + 1] = pack_bf16(dG.y, dU.y);
       }
-      stage_words16(half ? box1 : box0, cx.lane, w);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        stage128_put(box0, cx.lane, 4 * half + q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
   }
-  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
     map = 0;
-    x = 2 * (cx.n0 + 32 * c) + 32 * s;
+    x = 2 * (cx.n0 + 32 * c);
     y = cx.wrow0;
   }
   __device__ static void end(State&, const Params&, const EpiCtx&) {}
@@ -734,31 +744,38 @@ struct EpiSwiGLUBwdRowdot {
     float rv;
   };
   CODA_NO_PREFETCH
-  static constexpr int kInBoxes = 2;
+  static constexpr int kInBoxes = 2;  // ring bytes per chunk, filled by one 128-byte box (as EpiSwiGLUBwd)
+  static constexpr int kInLoads = 1;
   __device__ static bool has_input(const Params&, const EpiCtx&, int) { return true; }
-  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int b, int& map, int& x, int& y) {
+  __device__ static void in_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
     map = 0;
-    x = 2 * (cx.n0 + 32 * c) + 32 * b;
+    x = 2 * (cx.n0 + 32 * c);
     y = cx.wrow0;
   }
   static constexpr int kChunksPerStore = 1;
   static constexpr int kMaxSlots = 2;
   static constexpr int kStageBufs = 1;
   static constexpr int kInRingBytes = kRing;  // 4096: one chunk of inputs in flight; 8192: two
-  __device__ static int slots(const Params&) { return 2; }
+  __device__ static int slots(const Params&) { return 1; }
   __device__ static void begin(State& st, const Params& ep, const EpiCtx& cx) {
     st.dot = splat2(0.f);
     st.rv = (cx.row < cx.M && CODA_IN(cx, cx.row, cx.M)) ? ep.r[cx.row] : 0.f;
   }
   __device__ static void chunk(State& st, const Params&, const EpiCtx& cx, int, float (&acc)[32], const Pre&,
-                               uint32_t in, uint32_t box0, uint32_t box1) {
+                               uint32_t in, uint32_t box0, uint32_t) {
     const float2 rv = splat2(st.rv);
+    uint4 u[8];
+    box128_row(in, cx.lane, u);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      uint4 u[4];
-      box_row(in + half * kInBoxBytes, cx.lane, u);
       uint32_t w[16];
-      words16(u, w);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        w[4 * q] = u[4 * half + q].x;
+        w[4 * q + 1] = u[4 * half + q].y;
+        w[4 * q + 2] = u[4 * half + q].z;
+        w[4 * q + 3] = u[4 * half + q].w;
+      }
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         // r (dG, dU) from r dA; the row dot accumulates on the scaled values
@@ -771,12 +788,14 @@ struct EpiSwiGLUBwdRowdot {
         w[j] = pack_bf16(rdG.x, rdU.x);
         w[j + 1] = pack_bf16(rdG.y, rdU.y);
       }
-      stage_words16(half ? box1 : box0, cx.lane, w);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        stage128_put(box0, cx.lane, 4 * half + q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
   }
-  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int s, int& map, int& x, int& y) {
+  __device__ static void store_coord(const Params&, const EpiCtx& cx, int c, int, int& map, int& x, int& y) {
     map = 0;
-    x = 2 * (cx.n0 + 32 * c) + 32 * s;
+    x = 2 * (cx.n0 + 32 * c);
     y = cx.wrow0;
   }
   __device__ static void end(State& st, const Params& ep, const EpiCtx& cx) {

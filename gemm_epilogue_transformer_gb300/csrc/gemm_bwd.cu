@@ -16,9 +16,9 @@ int coda_gemm_swiglu_bwd(int M, int F, int K, const coda_bf16* dY, const coda_bf
   CODA_REQ_PTR16(gu);
   CODA_REQ_PTR16(dgu_out);
   CUtensorMap o;
-  if ((rc = make_out_map(&o, dgu_out, M, 2 * F, 2 * F))) return rc;
+  if ((rc = make_wide_map(&o, dgu_out, M, 2 * F, 2 * F))) return rc;
   CUtensorMap ig;
-  if ((rc = make_out_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
+  if ((rc = make_wide_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(gu);
   // dA = dY Wd^T: Wd is stored [F, K] = [N, K], a K-major B operand.
   if (K <= kDeepRingMaxK) {

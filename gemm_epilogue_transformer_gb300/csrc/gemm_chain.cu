@@ -69,8 +69,8 @@ int coda_gemm_swiglu_bwd_rowdot(int M, int F, int K, const coda_bf16* dY, const 
   CODA_REQ_PTR16(dgur_out);
   CODA_REQ_PTR4(pdot_out);
   CUtensorMap o, ig;
-  if ((rc = make_out_map(&o, dgur_out, M, 2 * F, 2 * F))) return rc;
-  if ((rc = make_out_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
+  if ((rc = make_wide_map(&o, dgur_out, M, 2 * F, 2 * F))) return rc;
+  if ((rc = make_wide_map(&ig, gu, M, 2 * F, 2 * F))) return rc;
   const auto* g = reinterpret_cast<const __nv_bfloat16*>(gu);
   // dA = dY Wd^T: Wd is stored [F, K] = [N, K], a K-major B operand.
   if (K <= kDeepRingMaxK) {

@@ -124,6 +124,18 @@ struct SharedOf<E, std::void_t<decltype(E::kSharedBytes)>> {
   static constexpr int value = E::kSharedBytes;
 };
 
+// TMA loads per chunk: kInBoxes (32 x 64-byte boxes) unless the epilogue
+// declares kInLoads = 1, one 32 x 128-byte box filling the same ring bytes
+// (the SwiGLU backward's 64 pre-activation columns per chunk).
+template <class E, class = void>
+struct InLoadsOf {
+  static constexpr int value = E::kInBoxes;
+};
+template <class E>
+struct InLoadsOf<E, std::void_t<decltype(E::kInLoads)>> {
+  static constexpr int value = E::kInLoads;
+};
+
 template <class Epi, int kCG>
 using CfgOf = Cfg<kCG, Epi::kInBoxes, Epi::kMaxSlots, InRingOf<Epi>::value, StageBufsOf<Epi>::value,
                   SharedOf<Epi>::value>;
@@ -271,6 +283,18 @@ __device__ __forceinline__ void stage_row32(uint32_t box, int r, const float (&v
   for (int q = 0; q < 4; ++q)
     stage_put(box, r, q, pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
               pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// Row r (0..31) of a 32 x 128B box laid out with the TMA 128-byte swizzle
+// (16-byte granule q of row r at granule q ^ (r mod 8)), as eight vectors; and
+// the matching staging write. Such a box must start on a 1024-byte boundary.
+__device__ __forceinline__ void box128_row(uint32_t box, int r, uint4 (&v)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = ld_shared_v4(box + r * 128 + ((q ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void stage128_put(uint32_t box, int r, int q, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  st_shared_v4(box + r * 128 + ((q ^ (r & 7)) << 4), a, b, c, d);
 }
 
 // Row r (0..31) of a 32 x 64B box laid out with the TMA 64-byte swizzle, as
@@ -617,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = in_base + slot * kIn * kInBoxBytes;
             mbar_arrive_expect_tx(bar, kIn * kInBoxBytes);
 #pragma unroll
-            for (int b = 0; b < kIn; ++b) {
+            for (int b = 0; b < InLoadsOf<Epi>::value; ++b) {
               int map, x, y;
               Epi::in_coord(ep, ic, it_c, b, map, x, y);
               if constexpr (kEpiEvictFirst)

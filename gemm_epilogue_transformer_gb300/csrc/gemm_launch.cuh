@@ -24,6 +24,14 @@ inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, in
                        static_cast<uint64_t>(ld) * 2u, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// A map of 32 x 64-element (128-byte) boxes with the 128-byte swizzle over a
+// row-major bf16 [rows, cols] tensor: the SwiGLU backward's pre-activation
+// input and its interleaved gradient output, 64 columns per chunk.
+inline int make_wide_map(CUtensorMap* m, const void* base, int rows, int cols, int ld) {
+  return make_map_bf16(m, base, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows),
+                       static_cast<uint64_t>(ld) * 2u, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // Checks shared by the fused bf16 entry points: non-negative dims, 8-element
 // granularity of N and K (16-byte rows), aligned operand pointers.
 inline int check_fused(const char* fn, int M, int N, int K, const void* A, const void* B) {
