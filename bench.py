@@ -211,6 +211,9 @@ class NvmlClocks:
         if self._t is not None:
             self._stop.set()
             self._t.join()
+        if self.nv is not None:
+            self.nv.nvmlShutdown()
+            self.nv = None
         if not self.samples:
             return {"sm_mhz": None, "samples": 0, "source": "nvml unavailable"}
         return {"sm_mhz": float(np.median(self.samples)), "sm_mhz_min": float(min(self.samples)),
