@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="time every fused operator against its unfused pair on all five workloads "
                          "(one JSON line per operator) instead of the headline step")
-    ap.add_argument("--reps", type=int, default=20, help="timed repetitions per operator in --suite (at least)")
+    ap.add_argument("--reps", type=int, default=50, help="timed repetitions per operator in --suite (at least)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="with --suite: raise each entry's repetitions until its timed region lasts this long")
     ap.add_argument("--only", default=None,
@@ -517,7 +517,7 @@ def main():
         # every other config, fused against unfused (median of alternating reps)
         del host, d_in, d_out, h_res, flush
         torch.cuda.empty_cache()
-        R = Runner(G, dev, reps=20)
+        R = Runner(G, dev, reps=50)
         entries = []
         for name in CONFIG_WORKLOADS:
             entries += run_workload(R, name)
@@ -576,6 +576,19 @@ class Runner:
         self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         self.peak_tf, self.peak_tf_sus, self.peak_bw, self.peak_kind = measured_peaks()
 
+    def _time_unflushed(self, fn, reps):
+        """Back-to-back launches of fn with no L2 flush between them: the other
+        cache regime (inputs may partly stay in L2)."""
+        import torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize(self.dev)
+        for s, e in ev:
+            s.record(self.stream)
+            fn()
+            e.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [s.elapsed_time(e) for s, e in ev]
+
     def _time(self, fns, reps):
         import torch
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fns]
@@ -616,8 +629,10 @@ class Runner:
         clk = NvmlClocks(self.dev.index or 0).start()
         t = self._time(fns, reps)
         c = clk.stop()
+        tn = self._time_unflushed(fused, min(reps, 200))
         fm, um = float(np.median(t[0])), float(np.median(t[1]))
         e = {"workload": workload, "op": op, "fused_ms": fm, "fused_min_ms": float(np.min(t[0])),
+             "fused_unflushed_ms": float(np.median(tn)),
              "unfused_ms": um, "unfused_min_ms": float(np.min(t[1])), "speedup_vs_unfused": um / fm,
              "fused_tflops": flops / (fm * 1e-3) / 1e12 if flops else None, "reps": reps,
              "kernels": launches, "sm_mhz": c.get("sm_mhz"), "clock_reasons": c.get("reasons"),
