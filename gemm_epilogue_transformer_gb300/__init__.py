@@ -16,7 +16,7 @@ import torch
 from . import _lib
 
 __all__ = [
-    "CodaError", "lib", "coda_init", "coda_device_status", "coda_set_wait_timeout_ns", "coda_set_cta_group", "coda_test_inject_missing_load",
+    "CodaError", "lib", "coda_init", "coda_device_status", "coda_set_wait_timeout_ns", "coda_set_cta_group", "coda_set_stream_k", "coda_test_inject_missing_load",
     "coda_num_col_tiles", "coda_num_row_tiles", "coda_gemm", "coda_gemm_res_rmsprep", "coda_rms_reduce",
     "coda_gemm_rowscale", "coda_gemm_swiglu", "coda_gemm_swiglu_bwd", "coda_rope_tables", "coda_gemm_rope",
     "coda_gemm_rope_bwd", "coda_gemm_ce_lse", "coda_ce_reduce", "coda_gemm_ce_bwd", "coda_gemm_rowdot",
@@ -134,6 +134,11 @@ def coda_set_wait_timeout_ns(ns: int):
 def coda_set_cta_group(g: int):
     """0 = automatic, 1 = single-SM 128 x 256 tiles, 2 = SM-pair 256 x 256 tiles."""
     _check(lib().coda_set_cta_group(int(g)))
+
+
+def coda_set_stream_k(mode: int):
+    """Stream-K split of the fused GEMMs: 0 = off, 1 = automatic (default), 2 = wherever it applies."""
+    _check(lib().coda_set_stream_k(int(mode)))
 
 
 def coda_test_inject_missing_load():

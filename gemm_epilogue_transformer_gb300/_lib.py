@@ -42,6 +42,7 @@ SIGNATURES = {
     "coda_device_status": (I, [I]),
     "coda_set_wait_timeout_ns": (I, [c_uint64]),
     "coda_set_cta_group": (I, [I]),
+    "coda_set_stream_k": (I, [I]),
     "coda_test_inject_missing_load": (I, []),
     "coda_num_col_tiles": (I, [I]),
     "coda_num_row_tiles": (I, [I]),

@@ -255,9 +255,11 @@ int coda_block_fwd_noalloc(const coda_block_t* b, coda_stream_t stream) {
   void* scratch = noalloc_scratch();
   if (!scratch) return CODA_ERR_CUDA;
   // the same launch sequence as coda_block_fwd, with the static array as its workspace (the
-  // forward touches only the partials, which the workspace layout places first)
+  // forward touches only the partials, which the workspace layout places first); the GEMMs
+  // run without the stream-K tail, whose per-stream workspace would be allocated
   coda_block_t c = *b;
   c.workspace = scratch;
+  NoAllocScope no_alloc;
   return coda_block_fwd(&c, stream);
 }
 

@@ -151,15 +151,57 @@ struct GemmShape {
   int M, N, K;
   int a_mn, b_mn;  // 0: K-major; 1: MN-major, 64-wide 2-D boxes; 2: MN-major, one 3-D box per stage
   int m_blocks, n_blocks, k_blocks, num_tiles, group_m;
-  // Work items: the first full_items are whole tiles in raster order; each of
-  // the remaining tiles (a partial last wave) is split into two 128-column
-  // halves so the last wave takes half a tile's time. num_items in total.
-  int full_items, num_items;
+  // Data-parallel work items, raster tiles from dp_first on: the first
+  // full_items are whole tiles; each of the remaining ones up to num_items (a
+  // partial last wave) is split into two 128-column halves so the last wave
+  // takes half a tile's time.
+  int dp_first, full_items, num_items;
+  // Stream-K tiles (sk_tiles > 0; then dp_first = sk_tiles and there are no
+  // half tiles): raster tiles 0 .. sk_tiles-1, one wave plus the leftover
+  // tiles, are dealt out as ranges of the flattened (tile, k-block) iteration
+  // space, sk_q + 1 k-blocks to each of the first sk_r clusters and sk_q to
+  // the others, so every cluster's work is the same. Each cluster runs its
+  // range before its data-parallel tiles, so the partials of split tiles are
+  // combined while later tiles' mainloops run. sk_q is at least k_blocks, so
+  // a tile is split at most once, at the boundary between two neighbouring
+  // clusters' ranges (see WorkCursor for the order a range is walked in);
+  // both pieces write their fp32 partial accumulator to sk_part, and the
+  // piece that arrives second (counted in sk_ctr, tagged with the launch's
+  // sk_epoch) adds the other's partial and runs the epilogue.
+  int sk_tiles, sk_q, sk_r;
+  int sk_rotate;       // 1: walk each range from its first tile boundary (see WorkCursor)
+  float4* sk_part;     // [boundary][side][CTA of the pair][epilogue warp][32 x 256 fp32], see sk_slot()
+  unsigned* sk_ctr;    // [boundary][CTA of the pair][epilogue warp] arrival words
+  unsigned sk_epoch;   // 1 .. 2^30 - 1, unique per launch on the workspace
   int seg_blocks;  // ceil(N / 128): second dimension of the [M, seg_blocks] partials
   int* status;                    // device status word (CODA_DEVST_* bits)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
   int inject;                     // test hook: 1 = producers skip their first stage fill
   float alpha;                    // FP8 mainloop: product of the operands' per-tensor scales
+};
+
+// One unit of a cluster's work: a tile (or a 128-column half tile) and the
+// range of k-blocks it accumulates. side -1: the whole reduction; side 0: the
+// first k-blocks of a tile split at the end of this cluster's stream-K range
+// (boundary bnd = this cluster); side 1: the last k-blocks of a tile split at
+// the start of it (bnd = the previous cluster).
+struct Work {
+  int m_blk, n0, ncols;
+  int kb0, kb1;
+  int side, bnd;
+};
+// Each role walks its cluster's work with its own cursor: the cluster's
+// stream-K range first, then the data-parallel items (t = cluster,
+// cluster + clusters, ...). With sk_rotate the range [lo, end) is walked
+// from its first tile boundary [pos, end), then the piece before it [lo, hi):
+// every cluster then starts at k-block 0 of some tile and all of them move
+// through K in step, as in the data-parallel waves, so the operand slices
+// read at one time are few. Without it ([lo, end) in order) the clusters'
+// k positions are spread over the whole reduction, which is faster while the
+// stream-K tiles' operands fit in L2 together and much slower once they do
+// not.
+struct WorkCursor {
+  int t, pos, end, lo, hi;
 };
 
 struct EpiCtx {
@@ -200,7 +242,7 @@ __device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_bl
 __device__ __forceinline__ void item_coords(int t, const GemmShape& p, int& m_blk, int& n0, int& ncols) {
   int n_blk;
   if (t < p.full_items) {
-    tile_coords(t, p, m_blk, n_blk);
+    tile_coords(p.dp_first + t, p, m_blk, n_blk);
     n0 = n_blk * BN;
     ncols = BN;
   } else {
@@ -219,6 +261,86 @@ __device__ __forceinline__ void tile_coords(int t, const GemmShape& p, int& m_bl
   if (gsz > p.group_m) gsz = p.group_m;
   m_blk = first_m + r % gsz;
   n_blk = r / gsz;
+}
+
+__device__ __forceinline__ void work_begin(const GemmShape& p, int cluster, WorkCursor& w) {
+  w.t = cluster;
+  w.pos = w.end = w.lo = w.hi = 0;
+  if (p.sk_tiles > 0) {
+    w.lo = cluster * p.sk_q + (cluster < p.sk_r ? cluster : p.sk_r);
+    w.end = w.lo + p.sk_q + (cluster < p.sk_r ? 1 : 0);
+    w.hi = p.sk_rotate ? (w.lo + p.k_blocks - 1) / p.k_blocks * p.k_blocks : w.lo;  // < end: range >= k_blocks
+    w.pos = w.hi;
+  }
+}
+// The cluster's next work unit; false when it has none left. Every role of
+// the cluster calls this in the same order and gets the same sequence.
+__device__ __forceinline__ bool work_next(const GemmShape& p, int cluster, int clusters, WorkCursor& w, Work& o) {
+  const bool rotated = w.pos >= w.end;  // the range's head [pos, end) is done: its first piece [lo, hi)
+  if (!rotated || w.lo < w.hi) {
+    const int s = rotated ? w.lo : w.pos;
+    const int e = rotated ? w.hi : w.end;
+    const int u = s / p.k_blocks;
+    const int base = u * p.k_blocks;
+    int n_blk;
+    tile_coords(u, p, o.m_blk, n_blk);
+    o.n0 = n_blk * BN;
+    o.ncols = BN;
+    o.kb0 = s - base;
+    o.kb1 = e - base < p.k_blocks ? e - base : p.k_blocks;
+    if (o.kb0 > 0) {
+      o.side = 1;
+      o.bnd = cluster - 1;
+    } else if (o.kb1 < p.k_blocks) {
+      o.side = 0;
+      o.bnd = cluster;
+    } else {
+      o.side = -1;
+      o.bnd = 0;
+    }
+    if (rotated)
+      w.lo = w.hi;
+    else
+      w.pos = base + o.kb1;
+    return true;
+  }
+  if (w.t < p.num_items) {
+    item_coords(w.t, p, o.m_blk, o.n0, o.ncols);
+    o.kb0 = 0;
+    o.kb1 = p.k_blocks;
+    o.side = -1;
+    o.bnd = 0;
+    w.t += clusters;
+    return true;
+  }
+  return false;
+}
+// Partial accumulator of one epilogue warp's 32 rows x 256 columns for the
+// piece `side` of the tile split at boundary `bnd`: chunk c (32 columns),
+// vector v (4 columns) of lane l's row at float4 index (c * 8 + v) * 32 + l,
+// so each warp-wide 16-byte access covers 512 contiguous bytes.
+__device__ __forceinline__ float4* sk_slot(const GemmShape& p, int kPair, int bnd, int side, uint32_t q, int ew) {
+  return p.sk_part + (static_cast<long>(((bnd * 2 + side) * kPair + static_cast<int>(q)) * 4 + ew) << 11);
+}
+__device__ __forceinline__ unsigned* sk_counter(const GemmShape& p, int kPair, int bnd, uint32_t q, int ew) {
+  return p.sk_ctr + ((bnd * kPair + static_cast<int>(q)) * 4 + ew);
+}
+// Count one piece's arrival at a split tile (lane 0 of the warp, after the
+// warp's partial writes and a fence). The word holds the launch's epoch in
+// its upper 30 bits and the arrivals in the lower 2; a word left by another
+// launch, also one that stopped part way, restarts the count. Returns the
+// number of arrivals including this one (2 = both pieces are in), or 0 if
+// the word could not be updated.
+__device__ __forceinline__ unsigned sk_arrive(unsigned* ctr, unsigned epoch) {
+  unsigned cur = atomicAdd(ctr, 0u);
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i) {
+    const unsigned want = (cur >> 2) == epoch ? cur + 1u : ((epoch << 2) | 1u);
+    const unsigned prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return want & 3u;
+    cur = prev;
+  }
+  return 0u;
 }
 
 // Bounded wait. Returns false (after flagging the status word and the CTA
@@ -440,12 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage = 1;
         issued = 1;
       }
-      for (int t = cluster_id; t < p.num_items && ok; t += num_clusters) {
-        int m_blk, n0, ncols;
-        item_coords(t, p, m_blk, n0, ncols);
-        const int m0 = m_blk * C::kTileM + static_cast<int>(q) * BM;
-        const int bcols = ncols / kPair;  // B columns this CTA loads
-        const int nb0 = n0 + static_cast<int>(q) * bcols;
+      WorkCursor wc;
+      work_begin(p, cluster_id, wc);
+      Work w;
+      while (ok && work_next(p, cluster_id, num_clusters, wc, w)) {
+        const int m0 = w.m_blk * C::kTileM + static_cast<int>(q) * BM;
+        const int bcols = w.ncols / kPair;  // B columns this CTA loads
+        const int nb0 = w.n0 + static_cast<int>(q) * bcols;
         // N-major B arrives in 64-column boxes (b_mn 1) or as one 3-D box of
         // kBLoad columns (b_mn 2); K-major B as one box of kBLoad rows (a half
         // tile reads past its columns: harmless extra bytes)
@@ -453,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx = kPair * (C::kABytes + (p.b_mn == 1 ? static_cast<uint32_t>(bcols * BK * 2) : C::kBBytes));
         // The k-loop is the kernel's critical path: keep it to the wait, the
         // expected-bytes arrive and the copies.
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag)) {
             ok = false;
             break;
@@ -528,14 +651,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = cluster_id; t < p.num_items && ok; t += num_clusters, ++local) {
-        const uint32_t idesc = t < p.full_items ? idesc_full : idesc_half;
+      WorkCursor wc;
+      work_begin(p, cluster_id, wc);
+      Work w;
+      for (; ok && work_next(p, cluster_id, num_clusters, wc, w); ++local) {
+        const uint32_t idesc = w.ncols == BN ? idesc_full : idesc_half;
         const int buf = local & 1;
         const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
         if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, p, abort_flag)) {
             ok = false;
             break;
@@ -547,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024u);
-            const uint32_t acc_in = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint32_t acc_in = (kb > w.kb0 || k > 0) ? 1u : 0u;
             if constexpr (kF8) {
               if constexpr (kCG == 2)
                 tc_mma_f8_pair(d_tmem, ad, bd, idesc, acc_in);
@@ -598,10 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       Epi::init_shared(ep, smem_u32(s_tab), static_cast<int>(threadIdx.x) - 64, p.status);
       asm volatile("bar.sync 1, 128;" ::: "memory");
     }
-    // Segment `seg` (128 columns) of work item tt; false if it lies past N.
-    auto make_ctx = [&](int tt, int seg, EpiCtx& cx) {
-      int n0, ncols;
-      item_coords(tt, p, cx.m_blk, n0, ncols);
+    // Segment `seg` (128 columns) of work unit wk; false if it lies past N.
+    auto make_ctx = [&](const Work& wk, int seg, EpiCtx& cx) {
+      cx.m_blk = wk.m_blk;
+      const int n0 = wk.n0;
       cx.status = p.status;
       cx.M = p.M;
       cx.N = p.N;
@@ -617,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cx.shared = C::kSharedBytes ? smem_u32(s_tab) : 0u;
       return cx.n0 < p.N;
     };
-    auto item_segs = [&](int tt) { return tt < p.full_items ? BN / BSEG : 1; };
+    auto item_segs = [&](const Work& wk) { return wk.ncols / BSEG; };
     constexpr int kSegChunks = BSEG / 32;
     int local = 0;
     int sbuf = 0;
@@ -629,12 +755,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t in_base = smem_u32(s_in) + ew * InRingOf<Epi>::value;
     uint32_t seq_used = 0;    // chunks consumed (all lanes)
     uint32_t seq_issued = 0;  // chunks issued (lane 0)
-    int it_t = cluster_id, it_s = 0, it_c = 0;  // issue cursor (lane 0)
+    int it_s = 0, it_c = 0;  // issue cursor (lane 0): segment and chunk of work unit iw
+    WorkCursor icur;
+    work_begin(p, cluster_id, icur);
+    Work iw;
+    bool it_live = work_next(p, cluster_id, num_clusters, icur, iw);
     EpiCtx ic;
-    bool ic_ok = it_t < p.num_items && make_ctx(it_t, 0, ic);
+    bool ic_ok = it_live && make_ctx(iw, 0, ic);
     auto issue_ahead = [&]() {
       if constexpr (kIn > 0) {
-        while (it_t < p.num_items && seq_issued < seq_used + C::kInSlots) {
+        while (it_live && seq_issued < seq_used + C::kInSlots) {
           if (ic_ok && Epi::has_input(ep, ic, it_c)) {
             const int slot = static_cast<int>(seq_issued % C::kInSlots);
             const uint32_t bar = in_bar(ew, slot);
@@ -653,11 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ic_ok || ++it_c == kSegChunks) {
             it_c = 0;
-            if (++it_s == item_segs(it_t)) {
+            if (++it_s == item_segs(iw)) {
               it_s = 0;
-              it_t += num_clusters;
+              it_live = work_next(p, cluster_id, num_clusters, icur, iw);
             }
-            ic_ok = it_t < p.num_items && make_ctx(it_t, it_s, ic);
+            ic_ok = it_live && make_ctx(iw, it_s, ic);
           }
         }
       }
@@ -666,17 +796,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     typename Epi::Pre pa, pb;
     EpiCtx cx;
+    // A stream-K piece that arrives first at its tile runs no epilogue: the
+    // input boxes issued ahead for the unit are waited for and dropped, in the
+    // order the ring issued them.
+    auto skip_inputs = [&](const Work& wk) {
+      if constexpr (kIn > 0) {
+        for (int seg = 0; seg < item_segs(wk); ++seg) {
+          EpiCtx sx;
+          if (!make_ctx(wk, seg, sx)) break;
+          for (int cs = 0; cs < kSegChunks; ++cs) {
+            if (!Epi::has_input(ep, sx, cs)) continue;
+            const int slot = static_cast<int>(seq_used % C::kInSlots);
+            if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
+            __syncwarp();
+            ++seq_used;
+            if (lane == 0) issue_ahead();
+          }
+        }
+      }
+    };
 
-    for (int t = cluster_id; t < p.num_items && ok; t += num_clusters, ++local) {
+    WorkCursor ecur;
+    work_begin(p, cluster_id, ecur);
+    Work w;
+    for (; ok && work_next(p, cluster_id, num_clusters, ecur, w); ++local) {
       const int buf = local & 1;
       const uint32_t tphase = static_cast<uint32_t>((local >> 1) & 1);
       if (!wait_bounded_sleep(tfull_bar(buf), tphase, p, abort_flag)) break;
       tc_fence_after();
+      // A piece of a split tile runs the epilogue only as the second piece to
+      // arrive, on the sum of both partials (two fp32 terms: the same sum
+      // whichever piece is second). If the other piece has already arrived
+      // (its arrival word shows one arrival of this launch) this one is
+      // second and goes straight on; otherwise it stores this warp's partial
+      // accumulator and counts its arrival, which tells it which it is.
+      const float4* partner = nullptr;
+      bool run = true;
+      if (w.side >= 0) {
+        unsigned* ctr = sk_counter(p, kPair, w.bnd, q, ew);
+        unsigned seen = 0;
+        if (lane == 0) seen = atomicAdd(ctr, 0u);
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        unsigned arrivals = 2;
+        if (seen != ((p.sk_epoch << 2) | 1u)) {
+          const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
+          float4* mine = sk_slot(p, kPair, w.bnd, w.side, q, ew) + lane;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float a[32];
+            tmem_ld32(tb + 32 * c, a);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              mine[(c * 8 + v) * 32] = make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) {
+            arrivals = sk_arrive(ctr, p.sk_epoch);
+            if (arrivals == 0) atomicOr(p.status, CODA_DEVST_SPLIT);
+          }
+          arrivals = __shfl_sync(0xffffffffu, arrivals, 0);
+        }
+        if (arrivals == 2) {
+          __threadfence();
+          partner = sk_slot(p, kPair, w.bnd, 1 - w.side, q, ew) + lane;
+        } else {
+          run = false;
+          skip_inputs(w);
+        }
+      }
       // One loop over the item's 8 (or 4) chunks; partial statistics close and
       // reopen at the 128-column segment boundary (chunk 4). A segment that
       // starts past N ends the item (only the last column block can).
-      const int nchunks = item_segs(t) * kSegChunks;
-      if (make_ctx(t, 0, cx)) {
+      const int nchunks = item_segs(w) * kSegChunks;
+      if (run && make_ctx(w, 0, cx)) {
         typename Epi::State st;
         Epi::begin(st, ep, cx);
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
@@ -692,6 +885,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float acc[32];
           tmem_ld32(tbase + 32 * c, acc);
+          if (partner != nullptr) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 o = __ldcg(partner + (c * 8 + v) * 32);
+              acc[4 * v] += o.x;
+              acc[4 * v + 1] += o.y;
+              acc[4 * v + 2] += o.z;
+              acc[4 * v + 3] += o.w;
+            }
+          }
           if (p.k_blocks == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
@@ -745,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < nchunks; c += 2) {
           if (c == kSegChunks) {
             Epi::end(st, ep, cx);
-            if (!make_ctx(t, 1, cx)) break;
+            if (!make_ctx(w, 1, cx)) break;
             Epi::begin(st, ep, cx);
             Epi::prefetch(ep, cx, 0, pa);
           }

@@ -17,6 +17,22 @@ namespace coda {
 // cannot hide one HBM round trip per chunk.
 constexpr int kDeepRingMaxK = 3072;
 
+// Stream-K split: only with at least this many k-blocks per tile (shorter
+// reductions gain little next to the partials' round trip).
+constexpr int kStreamKMinKBlocks = 16;
+// Whether the stream-K split is expected to beat the data-parallel schedule.
+// The latter's last wave costs a full tile time, or about 0.6 of one when it
+// runs as half tiles; the split costs rem / clusters of a tile time plus a
+// fixed overhead (the partials' round trip through L2 and the extra epilogue
+// passes of split tiles), measured on GB300 at 0.2-0.45 tile times for
+// 64 k-block tiles and near zero for 128-192 k-blocks: about 28 k-blocks.
+constexpr int kStreamKOverheadKBlocks = 28;
+inline bool stream_k_pays(int rem, int clusters, int N, int k_blocks) {
+  const double frac = static_cast<double>(rem) / clusters;
+  const double dp_tail = (2 * rem <= clusters && N > BSEG) ? 0.6 : 1.0;
+  return (dp_tail - frac) * k_blocks >= kStreamKOverheadKBlocks;
+}
+
 // Output map for a TMA store target: row-major bf16 [rows, cols], leading
 // dimension ld (elements), 32 x 32 boxes with the 64-byte swizzle.
 inline int make_out_map(CUtensorMap* m, const void* base, int rows, int cols, int ld) {
@@ -143,10 +159,46 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
     p.group_m = p.m_blocks < gm ? p.m_blocks : gm;
   }
   p.seg_blocks = (N + BSEG - 1) / BSEG;
-  // Wave balance: a last wave of `rem` tiles that fills at most half of the
-  // persistent clusters runs as 2 * rem half tiles (256 x 128 per pair) instead.
+  // Wave balance. With `rem` tiles past the last full wave of the persistent
+  // clusters, either one wave and those tiles run as stream-K work (their
+  // k-blocks dealt out evenly, ahead of the data-parallel tiles: every
+  // cluster ends together, at the cost of one partial-accumulator round trip
+  // through L2 per split tile), or, without it, a last wave of at most half
+  // the clusters runs as 2 * rem half tiles (256 x 128 per pair).
   const int rem = p.num_tiles % cmax;
-  if (rem > 0 && 2 * rem <= cmax && N > BSEG) {
+  p.dp_first = 0;
+  p.sk_tiles = p.sk_q = p.sk_r = p.sk_rotate = 0;
+  p.sk_part = nullptr;
+  p.sk_ctr = nullptr;
+  p.sk_epoch = 0;
+  const int skm = stream_k_setting();
+  if (rem > 0 && cmax >= 2 && p.num_tiles >= cmax + rem && p.k_blocks >= kStreamKMinKBlocks &&
+      (skm == 2 || (skm == 1 && stream_k_pays(rem, cmax, N, p.k_blocks)))) {
+    SkWorkspace ws;
+    if (sk_workspace(di, dev, stream, &ws)) {
+      p.sk_tiles = cmax + rem;
+      p.dp_first = p.sk_tiles;
+      const long long total = static_cast<long long>(p.sk_tiles) * p.k_blocks;
+      p.sk_q = static_cast<int>(total / cmax);
+      p.sk_r = static_cast<int>(total % cmax);
+      p.sk_part = static_cast<float4*>(ws.part);
+      p.sk_ctr = ws.ctr;
+      p.sk_epoch = ws.epoch;
+      // Walk the ranges in step (see WorkCursor) when the stream-K tiles'
+      // operands, spread over all of K, would take more than half of L2: the
+      // distinct row and column blocks of raster tiles 0 .. sk_tiles-1.
+      const int gm = p.group_m;
+      const int cols_b = (p.sk_tiles + gm - 1) / gm < p.n_blocks ? (p.sk_tiles + gm - 1) / gm : p.n_blocks;
+      const int rows_need = (p.sk_tiles + cols_b - 1) / cols_b;
+      const int rows_b = rows_need < p.m_blocks ? rows_need : p.m_blocks;
+      const double ws_bytes = (static_cast<double>(rows_b) * C::kTileM + static_cast<double>(cols_b) * BN) *
+                              static_cast<double>(p.k_blocks) * (kF8 ? 2 * BK : BK) * (kF8 ? 1.0 : 2.0);
+      p.sk_rotate = ws_bytes > 0.5 * static_cast<double>(di->l2_bytes) ? 1 : 0;
+    }
+  }
+  if (p.sk_tiles > 0) {
+    p.full_items = p.num_items = p.num_tiles - p.sk_tiles;
+  } else if (rem > 0 && 2 * rem <= cmax && N > BSEG) {
     p.full_items = p.num_tiles - rem;
     p.num_items = p.num_tiles + rem;
   } else {
@@ -158,7 +210,7 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.inject = take_injected_fault();
   p.alpha = alpha;
 
-  const int clusters = p.num_items < cmax ? p.num_items : cmax;
+  const int clusters = p.sk_tiles > 0 ? cmax : (p.num_items < cmax ? p.num_items : cmax);
   cfg.gridDim = dim3(clusters * kCG, 1, 1);
   // Programmatic dependent launch: the grid may be scheduled while the previous
   // kernel of the stream drains; the kernel waits for it before any global

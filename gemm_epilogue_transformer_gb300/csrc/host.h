@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/coda.h"
@@ -28,6 +29,31 @@ unsigned long long wait_timeout_ns();
 int cta_group_setting();
 // Consume the one-shot test fault set by coda_test_inject_missing_load().
 int take_injected_fault();
+// 0 = no stream-K split, 1 = where it is expected to pay (default), 2 = for
+// every shape it applies to (coda_set_stream_k).
+int stream_k_setting();
+
+// Stream-K workspace of one stream: fp32 partial accumulators of split tiles
+// and their arrival words, and this launch's epoch tag for those words.
+struct SkWorkspace {
+  void* part;
+  unsigned* ctr;
+  unsigned epoch;
+};
+// Bytes of partials a launch may use: one 256 KiB slot pair per SM
+// ((clusters - 1) boundaries x 2 pieces x 128 x 256 fp32 per CTA of a cluster).
+inline size_t sk_part_bytes(int sm_count) { return static_cast<size_t>(sm_count) * (size_t(256) << 10); }
+// The calling stream's workspace on the current device, created by its first
+// stream-K launch (cudaMalloc, arrival words zeroed on the stream); false when
+// the stream is being captured, the thread is inside a NoAllocScope, or the
+// workspace cannot be had, and the launch then runs without the stream-K split.
+bool sk_workspace(const DeviceInfo* di, int dev, cudaStream_t stream, SkWorkspace* out);
+// While one exists on a thread, launches from that thread allocate nothing
+// (no stream-K workspace is created or used).
+struct NoAllocScope {
+  NoAllocScope();
+  ~NoAllocScope();
+};
 
 // The C ABI's opaque stream handle as a CUDA stream.
 inline cudaStream_t as_stream(coda_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }

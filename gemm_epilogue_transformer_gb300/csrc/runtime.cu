@@ -17,6 +17,7 @@ static thread_local char g_err[1024] = "";
 static std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 static std::atomic<int> g_cta_group{0};
 static std::atomic<int> g_inject{0};
+static std::atomic<int> g_stream_k{1};
 
 // The device status word (CODA_DEVST_* bits). Kernels receive its device
 // address, obtained per device with cudaGetSymbolAddress.
@@ -82,6 +83,105 @@ const DeviceInfo* current_device() {
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 int cta_group_setting() { return g_cta_group; }
 int take_injected_fault() { return g_inject.exchange(0); }
+int stream_k_setting() { return g_stream_k; }
+
+// ------------------------------------------------- stream-K workspaces
+// One per (device, stream handle), created by the stream's first stream-K
+// launch and kept for the life of the process (one CUDA context per device,
+// as for every per-device cache here). Launches on one stream run in order,
+// so they can share its workspace; different streams never share one.
+namespace {
+struct SkEntry {
+  int dev;
+  cudaStream_t stream;
+  unsigned long long sid;  // cudaStreamGetId of the stream the handle named when last used
+  char* mem;               // partials, then the arrival words
+  unsigned epoch;
+};
+constexpr int kMaxSkStreams = 64;
+std::mutex g_sk_mu;
+SkEntry g_sk[kMaxSkStreams];
+int g_sk_n = 0;
+thread_local int tl_no_alloc = 0;
+
+size_t sk_ctr_bytes(int sm_count) { return static_cast<size_t>(sm_count) * 4 * sizeof(unsigned); }
+}  // namespace
+
+NoAllocScope::NoAllocScope() { ++tl_no_alloc; }
+NoAllocScope::~NoAllocScope() { --tl_no_alloc; }
+
+bool sk_workspace(const DeviceInfo* di, int dev, cudaStream_t stream, SkWorkspace* out) {
+  if (tl_no_alloc) return false;
+  // a captured launch would bake this launch's epoch into every replay
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return false;
+  unsigned long long sid = 0;
+  if (cudaStreamGetId(stream, &sid) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const size_t part = sk_part_bytes(di->sm_count), ctr = sk_ctr_bytes(di->sm_count);
+  std::lock_guard<std::mutex> lk(g_sk_mu);
+  SkEntry* e = nullptr;
+  for (int i = 0; i < g_sk_n; ++i)
+    if (g_sk[i].dev == dev && g_sk[i].stream == stream) e = &g_sk[i];
+  if (e && e->sid != sid) {
+    // The handle now names a new stream (the old one was destroyed): launches
+    // of the old stream may still be running on this workspace.
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    const cudaError_t r = cudaDeviceSynchronize();
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (r != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    e->sid = sid;
+  }
+  if (!e) {
+    if (g_sk_n == kMaxSkStreams) return false;
+    void* mem = nullptr;
+    // relaxed: the allocation must not disturb another thread's capture
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    cudaError_t r = cudaMalloc(&mem, part + ctr);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (r != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    r = cudaMemsetAsync(static_cast<char*>(mem) + part, 0, ctr, stream);
+    if (r != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(mem);
+      return false;
+    }
+    e = &g_sk[g_sk_n++];
+    e->dev = dev;
+    e->stream = stream;
+    e->sid = sid;
+    e->mem = static_cast<char*>(mem);
+    e->epoch = 0;
+  }
+  // Epoch tags are 30 bits; before they wrap, the words are zeroed on the
+  // stream so no word left from 2^30 launches ago can match a new tag.
+  if (++e->epoch >= (1u << 30)) {
+    if (cudaMemsetAsync(e->mem + part, 0, ctr, stream) != cudaSuccess) {
+      cudaGetLastError();
+      --e->epoch;
+      return false;
+    }
+    e->epoch = 1;
+  }
+  out->part = e->mem;
+  out->ctr = reinterpret_cast<unsigned*>(e->mem + part);
+  out->epoch = e->epoch;
+  return true;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -194,6 +294,12 @@ int coda_set_wait_timeout_ns(unsigned long long ns) {
 int coda_set_cta_group(int g) {
   if (g < 0 || g > 2) return fail(CODA_ERR_INVALID, "coda_set_cta_group: %d is not 0, 1 or 2", g);
   g_cta_group = g;
+  return CODA_OK;
+}
+
+int coda_set_stream_k(int mode) {
+  if (mode < 0 || mode > 2) return fail(CODA_ERR_INVALID, "coda_set_stream_k: %d is not 0, 1 or 2", mode);
+  g_stream_k = mode;
   return CODA_OK;
 }
 

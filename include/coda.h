@@ -13,7 +13,10 @@
  *
  * Conventions for every entry point
  *   - Tensors are device pointers, allocated and owned by the caller. The
- *     library never allocates, frees or retains caller memory.
+ *     library never allocates, frees or retains caller memory. Its own device
+ *     memory is the status word, the static array of coda_block_fwd_noalloc
+ *     and one stream-K workspace per stream that uses the split
+ *     (coda_set_stream_k), each kept until the process exits.
  *   - bf16 tensors are passed as coda_bf16 (uint16_t bit patterns), row-major
  *     and contiguous unless a leading dimension (in elements) is given.
  *     Statistics are fp32, labels int32. Weights are [K, N] row-major.
@@ -71,6 +74,7 @@ extern "C" {
 #define CODA_DEVST_TIMEOUT 1   /* a bounded in-kernel wait ran out            */
 #define CODA_DEVST_BAD_LABEL 2 /* a cross-entropy label was outside [0, V)    */
 #define CODA_DEVST_BOUNDS 4    /* checked build only: an epilogue's direct global access fell outside its tensor */
+#define CODA_DEVST_SPLIT 8     /* a split tile's arrival word could not be updated; that tile is not written */
 
 typedef uint16_t coda_bf16;
 typedef void* coda_stream_t;
@@ -99,6 +103,32 @@ int coda_set_wait_timeout_ns(unsigned long long ns);
  * Results are identical up to fp32 accumulation order. Other values are
  * rejected with CODA_ERR_INVALID. */
 int coda_set_cta_group(int g);
+
+/* Stream-K work split for every later launch on this process. A fused GEMM
+ * runs as persistent tile loops, one per SM (pair); when the tile count is
+ * not a multiple of their number, the last wave leaves most of the GPU idle.
+ * With the split on, one wave plus the leftover tiles are instead shared out
+ * as equal ranges of k-blocks, run before the remaining whole tiles, so
+ * every SM (pair) does the same work; a tile whose k-blocks fall in two
+ * ranges is accumulated in two pieces, whose fp32 partials meet in a
+ * per-stream workspace, and the piece that finishes second adds them and
+ * runs the epilogue.
+ *   0 = off: the last wave runs as whole tiles or as 128-column half tiles;
+ *   1 = automatic (default): the split where it is expected to be faster
+ *       (at least 16 k-blocks of 64, and a last wave that leaves enough of
+ *       the GPU idle);
+ *   2 = whenever it applies (K >= 1024 and more tiles than one wave).
+ * Other values are rejected with CODA_ERR_INVALID.
+ * Results stay deterministic: a split tile's accumulator is the fp32 sum of
+ * its two pieces, the same whichever finishes first. They differ from the
+ * data-parallel schedule's only in fp32 accumulation order.
+ * Workspace: a stream's first launch that uses the split allocates its
+ * workspace (256 KiB per SM, about 38 MiB on GB300, with cudaMalloc) and
+ * zeroes its arrival words on the stream; it is kept until the process
+ * exits, one per stream handle (at most 64). Launches made while the stream
+ * is being captured into a CUDA graph, and those of coda_block_fwd_noalloc,
+ * never use the split, so they allocate nothing and capture no workspace. */
+int coda_set_stream_k(int mode);
 
 /* Test hook for the failure-detection path: the next fused-GEMM launch from
  * this process skips the producers' first stage fill, so the MMA issuer's

@@ -89,9 +89,12 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.coda_rms_reduce(8, 0, 8, good, 1e-6, good, None) == INVALID
     assert lib.coda_rms_reduce(8, 2, 8, good, -1.0, good, None) == INVALID
     assert lib.coda_set_wait_timeout_ns(10) == INVALID
-    # tile variants: 0 (automatic), 1, 2 and 4 only; the setting is process-wide
+    # tile variants: 0 (automatic), 1 and 2 only; the setting is process-wide
     assert [lib.coda_set_cta_group(g) for g in (3, 4, 5, -1)] == [INVALID] * 4
     assert [lib.coda_set_cta_group(g) for g in (2, 1, 0)] == [0] * 3
+    # stream-K tail: 0 (off), 1 (automatic) and 2 (wherever it applies) only
+    assert [lib.coda_set_stream_k(m) for m in (3, -1)] == [INVALID] * 2
+    assert [lib.coda_set_stream_k(m) for m in (0, 2, 1)] == [0] * 3
     assert lib.coda_unfused_rmsnorm_bwd(8, 65536, good, good, good, good, good, good, None) == UNSUPPORTED
     # empty problems are no-ops that never touch the device
     assert lib.coda_gemm(0, 8, 8, None, 8, 0, None, 8, 0, None, 8, None) == 0

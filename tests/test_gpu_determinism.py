@@ -5,8 +5,9 @@ Every launch of a variant computes the same tiles with the same K order and
 the same epilogue program; only the assignment of tiles to persistent CTAs
 and the timing differ. Any difference between two launches would be a race in
 the barrier protocol (a stage overwritten before its MMAs finished, an
-accumulator read before it was complete). Shapes span several waves of
-persistent clusters, ragged edges and the half-tile tail items."""
+accumulator read before it was complete, a split tile's partial read before
+it was written). Shapes span several waves of persistent clusters, ragged
+edges, the half-tile tail items and the stream-K split."""
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +43,19 @@ def _cases(coda):
     gam1 = (1 + 0.1 * torch.randn(1024, device="cuda", generator=g)).bfloat16()
     H, Wv = bf(1200, 512), bf(512, 5000, std=512 ** -0.5)
     y = torch.randint(0, 5000, (1200,), device="cuda", dtype=torch.int32, generator=g)
+    Ak, Bk = bf(1800, 1096), bf(1096, 3400, std=1096 ** -0.5)
+    GUk = bf(1800, 2 * 3400)
+    Wdk = bf(3400, 1096, std=1096 ** -0.5)
+
+    def streamk(fn):
+        # the stream-K split forced on: split tiles meet through the workspace
+        def run():
+            coda.coda_set_stream_k(2)
+            try:
+                return fn()
+            finally:
+                coda.coda_set_stream_k(1)
+        return run
     A8 = torch.randint(0, 256, (2048, 1024), device="cuda", dtype=torch.uint8, generator=g) & 0x77
     B8 = torch.randint(0, 256, (3072, 1024), device="cuda", dtype=torch.uint8, generator=g) & 0x77
     return {
@@ -55,6 +69,8 @@ def _cases(coda):
         "rmsnorm_bwd": lambda: coda.coda_gemm_rmsnorm_bwd(z, W1, x, gam1, r, sv),
         "ce_lse": lambda: coda.coda_gemm_ce_lse(H, Wv, y),
         "fp8": lambda: coda.coda_gemm_fp8(A8, B8, 0.03),
+        "gemm_streamk": streamk(lambda: coda.coda_gemm(Ak, Bk)),
+        "swiglu_bwd_streamk": streamk(lambda: coda.coda_gemm_swiglu_bwd(Ak, Wdk, GUk)),
     }
 
 
