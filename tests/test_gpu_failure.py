@@ -72,14 +72,32 @@ def _fp8_case(coda):
     return run, ref
 
 
-@pytest.mark.parametrize("case", [_rope_case, _swiglu_bwd_case, _fp8_case],
-                         ids=["rope_shared_tables", "swiglu_bwd_inputs", "fp8_mainloop"])
+def _streamk_case(coda):
+    """More tiles than one wave with the stream-K split forced on: the abort
+    hits a launch whose split tiles would meet through the workspace, and the
+    next launch (a new epoch for the arrival words) is correct."""
+    p = gen.swiglu_problem(1800, 1096, 1700, seed=7)
+    X, W = dev_bf16(p["X"]), dev_bf16(p["Wgu"])
+
+    def run():
+        coda.coda_set_stream_k(2)
+        try:
+            return coda.coda_gemm(X, W)
+        finally:
+            coda.coda_set_stream_k(1)
+    ref = O.matmul(O.bf16(p["X"]), O.bf16(p["Wgu"]))
+    return run, ref
+
+
+@pytest.mark.parametrize("case", [_rope_case, _swiglu_bwd_case, _fp8_case, _streamk_case],
+                         ids=["rope_shared_tables", "swiglu_bwd_inputs", "fp8_mainloop", "stream_k_split"])
 @pytest.mark.parametrize("cg", [1, 2], ids=["cta1", "cta2"])
 def test_abort_with_epilogue_inputs_in_flight(coda, cg, case):
     """The same missing fill in a kernel whose epilogue warps filled a shared
     table first (RoPE), in one whose epilogue warps already have TMA input
-    boxes in flight (SwiGLU pre-activations), and in the FP8 mainloop: the
-    abort path drains what is in flight, and the context stays usable."""
+    boxes in flight (SwiGLU pre-activations), in the FP8 mainloop and with the
+    stream-K split: the abort path drains what is in flight, and the context
+    stays usable."""
     run, ref = case(coda)
     try:
         coda.coda_set_cta_group(cg)
