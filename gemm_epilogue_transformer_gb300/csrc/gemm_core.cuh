@@ -172,6 +172,8 @@ struct GemmShape {
   int sk_rotate;       // 1: walk each range from its first tile boundary (see WorkCursor)
   float4* sk_part;     // [boundary][side][CTA of the pair][epilogue warp][32 x 256 fp32], see sk_slot()
   unsigned* sk_ctr;    // [boundary][CTA of the pair][epilogue warp] arrival words
+  long sk_part_f4;     // extents of the two (float4s, words), for the checked build
+  int sk_ctr_n;
   unsigned sk_epoch;   // 1 .. 2^30 - 1, unique per launch on the workspace
   int seg_blocks;  // ceil(N / 128): second dimension of the [M, seg_blocks] partials
   int* status;                    // device status word (CODA_DEVST_* bits)
@@ -319,11 +321,11 @@ __device__ __forceinline__ bool work_next(const GemmShape& p, int cluster, int c
 // piece `side` of the tile split at boundary `bnd`: chunk c (32 columns),
 // vector v (4 columns) of lane l's row at float4 index (c * 8 + v) * 32 + l,
 // so each warp-wide 16-byte access covers 512 contiguous bytes.
-__device__ __forceinline__ float4* sk_slot(const GemmShape& p, int kPair, int bnd, int side, uint32_t q, int ew) {
-  return p.sk_part + (static_cast<long>(((bnd * 2 + side) * kPair + static_cast<int>(q)) * 4 + ew) << 11);
+__device__ __forceinline__ long sk_slot(int kPair, int bnd, int side, uint32_t q, int ew) {
+  return static_cast<long>(((bnd * 2 + side) * kPair + static_cast<int>(q)) * 4 + ew) << 11;
 }
-__device__ __forceinline__ unsigned* sk_counter(const GemmShape& p, int kPair, int bnd, uint32_t q, int ew) {
-  return p.sk_ctr + ((bnd * kPair + static_cast<int>(q)) * 4 + ew);
+__device__ __forceinline__ int sk_counter(int kPair, int bnd, uint32_t q, int ew) {
+  return (bnd * kPair + static_cast<int>(q)) * 4 + ew;
 }
 // Count one piece's arrival at a split tile (lane 0 of the warp, after the
 // warp's partial writes and a fence). The word holds the launch's epoch in
@@ -832,15 +834,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator and counts its arrival, which tells it which it is.
       const float4* partner = nullptr;
       bool run = true;
-      if (w.side >= 0) {
-        unsigned* ctr = sk_counter(p, kPair, w.bnd, q, ew);
+      const long own_slot = w.side >= 0 ? sk_slot(kPair, w.bnd, w.side, q, ew) : 0;
+      const long other_slot = w.side >= 0 ? sk_slot(kPair, w.bnd, 1 - w.side, q, ew) : 0;
+      const int ctr_i = w.side >= 0 ? sk_counter(kPair, w.bnd, q, ew) : 0;
+      if (w.side >= 0 && !(CODA_IN_ST(p.status, own_slot + 2047, p.sk_part_f4) &&
+                           CODA_IN_ST(p.status, other_slot + 2047, p.sk_part_f4) &&
+                           CODA_IN_ST(p.status, ctr_i, p.sk_ctr_n))) {
+        run = false;  // checked build only: the tile is left unwritten, CODA_DEVST_BOUNDS is set
+        skip_inputs(w);
+      } else if (w.side >= 0) {
+        unsigned* ctr = p.sk_ctr + ctr_i;
         unsigned seen = 0;
         if (lane == 0) seen = atomicAdd(ctr, 0u);
         seen = __shfl_sync(0xffffffffu, seen, 0);
         unsigned arrivals = 2;
         if (seen != ((p.sk_epoch << 2) | 1u)) {
           const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * ew) << 16) + static_cast<uint32_t>(buf * BN);
-          float4* mine = sk_slot(p, kPair, w.bnd, w.side, q, ew) + lane;
+          float4* mine = p.sk_part + own_slot + lane;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             float a[32];
@@ -859,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (arrivals == 2) {
           __threadfence();
-          partner = sk_slot(p, kPair, w.bnd, 1 - w.side, q, ew) + lane;
+          partner = p.sk_part + other_slot + lane;
         } else {
           run = false;
           skip_inputs(w);

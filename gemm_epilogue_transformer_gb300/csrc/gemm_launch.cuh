@@ -170,6 +170,8 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
   p.sk_tiles = p.sk_q = p.sk_r = p.sk_rotate = 0;
   p.sk_part = nullptr;
   p.sk_ctr = nullptr;
+  p.sk_part_f4 = 0;
+  p.sk_ctr_n = 0;
   p.sk_epoch = 0;
   const int skm = stream_k_setting();
   if (rem > 0 && cmax >= 2 && p.num_tiles >= cmax + rem && p.k_blocks >= kStreamKMinKBlocks &&
@@ -183,6 +185,8 @@ int launch_variant(const char* fn, const DeviceInfo* di, int M, int N, int K, co
       p.sk_r = static_cast<int>(total % cmax);
       p.sk_part = static_cast<float4*>(ws.part);
       p.sk_ctr = ws.ctr;
+      p.sk_part_f4 = static_cast<long>(sk_part_bytes(di->sm_count) / sizeof(float4));
+      p.sk_ctr_n = sk_ctr_words(di->sm_count);
       p.sk_epoch = ws.epoch;
       // Walk the ranges in step (see WorkCursor) when the stream-K tiles'
       // operands, spread over all of K, would take more than half of L2: the

@@ -43,6 +43,8 @@ struct SkWorkspace {
 // Bytes of partials a launch may use: one 256 KiB slot pair per SM
 // ((clusters - 1) boundaries x 2 pieces x 128 x 256 fp32 per CTA of a cluster).
 inline size_t sk_part_bytes(int sm_count) { return static_cast<size_t>(sm_count) * (size_t(256) << 10); }
+// Arrival words: (clusters - 1) boundaries x 4 epilogue warps per CTA of a cluster.
+inline int sk_ctr_words(int sm_count) { return sm_count * 4; }
 // The calling stream's workspace on the current device, created by its first
 // stream-K launch (cudaMalloc, arrival words zeroed on the stream); false when
 // the stream is being captured, the thread is inside a NoAllocScope, or the

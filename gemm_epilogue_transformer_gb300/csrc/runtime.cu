@@ -104,7 +104,7 @@ SkEntry g_sk[kMaxSkStreams];
 int g_sk_n = 0;
 thread_local int tl_no_alloc = 0;
 
-size_t sk_ctr_bytes(int sm_count) { return static_cast<size_t>(sm_count) * 4 * sizeof(unsigned); }
+size_t sk_ctr_bytes(int sm_count) { return static_cast<size_t>(sk_ctr_words(sm_count)) * sizeof(unsigned); }
 }  // namespace
 
 NoAllocScope::NoAllocScope() { ++tl_no_alloc; }

@@ -1,8 +1,9 @@
 """The checked build (libcoda_checked.so, compiled with CODA_CHECKED=1) tests
 the index of every direct global load and store of the fused epilogues against
 the extent of the tensor it touches and sets CODA_DEVST_BOUNDS instead of
-making the access. This test reruns the fused, edge, sentinel, block-chain and
-FP8 parity suites in a child process that loads the checked build: every
+making the access (the stream-K split's partial accumulators and arrival words
+included). This test reruns the fused, edge, sentinel, block-chain, FP8 and
+stream-K parity suites in a child process that loads the checked build: every
 parity assertion must still hold and no read of the status word may show the
 bounds bit (tests/conftest.py fails any such read)."""
 import os
@@ -15,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_fused.py", "tests/test_gpu_edges.py", "tests/test_gpu_sentinels.py",
-          "tests/test_gpu_block.py", "tests/test_gpu_fp8.py"]
+          "tests/test_gpu_block.py", "tests/test_gpu_fp8.py", "tests/test_gpu_streamk.py"]
 
 
 def test_parity_suites_on_the_checked_build():
