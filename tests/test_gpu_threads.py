@@ -2,7 +2,8 @@
 
 A fresh process starts four threads before any kernel of the library has run,
 so the per-kernel first-use set-up (shared-memory attribute, cluster
-occupancy query) and the launch settings are exercised under concurrency.
+occupancy query), the creation of each stream's stream-K workspace and the
+launch settings are exercised under concurrency.
 Each thread runs a mix of fused kernels and auxiliary reductions on its own
 stream; one thread keeps switching the tile setting between automatic and
 SM pairs (the same variant at these shapes, so bit-identical results). Afterwards the same calls
@@ -25,6 +26,7 @@ CHILD = textwrap.dedent("""
     import gemm_epilogue_transformer_gb300 as coda
 
     coda.coda_init(0)
+    coda.coda_set_stream_k(2)  # the split wherever it applies: only the 1800 x 3400 x 1096 GEMM below
     g = torch.Generator(device="cuda").manual_seed(5)
     def bf(*s, std=1.0):
         return (torch.randn(*s, device="cuda", generator=g) * std).bfloat16()
@@ -35,6 +37,7 @@ CHILD = textwrap.dedent("""
     Wgu = bf(384, 2 * 520, std=384 ** -0.5)
     H, Wv = bf(600, 256), bf(256, 3000, std=256 ** -0.5)
     y = torch.randint(0, 3000, (600,), device="cuda", dtype=torch.int32, generator=g)
+    Ak, Bk = bf(1800, 1096), bf(1096, 3400, std=1096 ** -0.5)
     torch.cuda.synchronize()
 
     def step():
@@ -46,7 +49,8 @@ CHILD = textwrap.dedent("""
         a, gu = coda.coda_gemm_swiglu(X, Wgu, want_gu=True)
         pm, ps, pa, t = coda.coda_gemm_ce_lse(H, Wv, y)
         lse, lrow, lmean, am = coda.coda_ce_reduce(pm, ps, pa, t)
-        return [h1, h2, r, Y, q, a, gu, lse, lrow, lmean, am]
+        Ck = coda.coda_gemm(Ak, Bk)   # stream-K split: each stream's first use creates its workspace
+        return [h1, h2, r, Y, q, a, gu, lse, lrow, lmean, am, Ck]
 
     N_THREADS, REPS = 4, 6
     results = [[] for _ in range(N_THREADS)]
