@@ -71,3 +71,31 @@ def test_tiny_rms_chain_graph_replay(coda):
     torch.cuda.synchronize()
     for k, v in out.items():
         assert torch.equal(v, ref[k]), k
+
+
+def test_capture_runs_without_the_split(coda):
+    """A launch captured into a CUDA graph never uses the stream-K split (its
+    arrival-word epoch would be baked into every replay): with the split forced
+    on, the replayed GEMM gives the data-parallel schedule's bits, not those of
+    the direct launch that used the split."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(17)
+    A = (torch.randn(1800, 1096, device="cuda", generator=g)).bfloat16()
+    B = (torch.randn(1096, 3400, device="cuda", generator=g) * 1096 ** -0.5).bfloat16()
+    C = torch.empty(1800, 3400, dtype=torch.bfloat16, device="cuda")
+    try:
+        coda.coda_set_stream_k(0)
+        dp = coda.coda_gemm(A, B).clone()
+        coda.coda_set_stream_k(2)
+        sk = coda.coda_gemm(A, B).clone()
+        torch.cuda.synchronize()
+        assert not torch.equal(dp, sk), "the direct launch did not use the split"
+        graph = _capture(lambda: coda.coda_gemm(A, B, out=C))
+        C.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(C, dp), "the captured launch used the split"
+    finally:
+        coda.coda_set_stream_k(1)
+    assert coda.coda_device_status(clear=True) == 0
+

@@ -53,3 +53,32 @@ def test_block_fwd_noalloc_limit(coda):
     b.M, b.d, b.F = 1 << 20, 1024, 1024   # 2^20 rows x 8 blocks x 4 B = 32 MiB of partials
     assert coda.lib().coda_block_fwd_noalloc(b, None) == -2  # CODA_ERR_UNSUPPORTED, nothing launched
     assert b"static scratch" in coda.lib().coda_last_error()
+
+
+def test_block_fwd_noalloc_never_splits(coda):
+    """The no-allocation forward never takes the stream-K split, whose per-stream
+    workspace would be allocated: with the split forced on, it gives the bits of
+    the workspace variant run without the split, at a size where the split
+    applies (1536 rows: the 3456-wide QKV GEMM has 84 SM-pair tiles and the
+    4608-wide gate/up GEMM 108, on 76 pairs, with K = 1152)."""
+    import torch
+    M, d, F, hd, S = 1536, 1152, 2304, 128, 512
+    p = gen.block_problem(M, d, F, seed=23, with_bwd=False)
+    t = {k: dev_bf16(v) for k, v in p.items()}
+    cos, sin = coda.coda_rope_tables(S, hd, THETA)
+    names = ("h1", "h2", "gu", "qkv", "a", "r1", "r2")
+    try:
+        coda.coda_set_stream_k(0)
+        ref = coda.CodaBlock(t, hd, 2 * d, cos, sin, EPS).fwd()
+        coda.coda_set_stream_k(2)
+        split = coda.CodaBlock(t, hd, 2 * d, cos, sin, EPS).fwd()
+        blk = coda.CodaBlock(t, hd, 2 * d, cos, sin, EPS)
+        blk.fwd_noalloc()
+        torch.cuda.synchronize()
+    finally:
+        coda.coda_set_stream_k(1)
+    assert not torch.equal(split.gu, ref.gu), "the workspace variant did not use the split"
+    for k in names:
+        assert torch.equal(getattr(blk, k), getattr(ref, k)), f"{k}: the no-allocation forward used the split"
+    assert coda.coda_device_status(clear=True) == 0
+
