@@ -176,3 +176,47 @@ def test_fp8(coda, cta_group):
     _, (R,) = _modes(coda, lambda: coda.coda_gemm_rope_fp8(A8, B8, alpha, c, s, hd, rc))
     assert_bf16(R, O.rope(O.matmul(a, b.T), np.arange(M) % S, hd, THETA, rc), "fp8 rope (stream-K)")
     assert coda.coda_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_split_matches_data_parallel_on_random_shapes(coda, cta_group, seed):
+    """Random ragged shapes with one to three waves of tiles and 16-80 k-blocks:
+    the split changes only the fp32 accumulation order, so every bf16 output
+    equals the data-parallel one or differs by one bf16 rounding step (the two
+    fp32 sums of O(1) outputs agree to far better than 2^-8), and the two runs
+    under the split agree bit for bit."""
+    import torch
+    rng = np.random.default_rng(1000 + seed)
+    tile_m = 256 if cta_group == 0 else 128
+    clusters = 76 if cta_group == 0 else 152
+    for _ in range(4):
+        M = int(rng.integers(2, 17)) * tile_m - int(rng.integers(0, 100))
+        mb = -(-M // tile_m)
+        nb = int(rng.integers(clusters // mb + 1, 3 * clusters // mb + 2))
+        N = max(8, (nb * 256 - int(rng.integers(0, 32)) * 8))
+        K = int(rng.integers(16, 81)) * 64 - int(rng.integers(0, 8)) * 8
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        A = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+        B = (torch.randn(K, N, device="cuda", generator=g) * K ** -0.5).bfloat16()
+        dp, sk = _modes_raw(coda, lambda: coda.coda_gemm(A, B))
+        d = (sk.float() - dp.float()).abs()
+        # one bf16 step of the output, with an absolute floor for outputs near zero,
+        # where the fp32 sums' (K^(1/2) 2^-24-sized) difference can exceed a step
+        step = (dp.float().abs() * 2.0 ** -7).clamp_min(1e-4)
+        assert bool((d <= step).all()), f"{M}x{N}x{K}: split and data-parallel differ by more than one bf16 step"
+    assert coda.coda_device_status(clear=True) == 0
+
+
+def _modes_raw(coda, fn):
+    """fn() without the split and with it (twice, checked equal); raw tensors."""
+    import torch
+    coda.coda_set_stream_k(0)
+    dp = fn().clone()
+    coda.coda_set_stream_k(2)
+    sk = fn().clone()
+    sk2 = fn().clone()
+    coda.coda_set_stream_k(1)
+    torch.cuda.synchronize()
+    assert torch.equal(sk, sk2), "two stream-K launches differ"
+    return dp, sk
+
