@@ -220,3 +220,33 @@ def _modes_raw(coda, fn):
     assert torch.equal(sk, sk2), "two stream-K launches differ"
     return dp, sk
 
+
+@pytest.mark.parametrize("K", [1024, 1032], ids=["kb16", "kb17_ragged"])
+@pytest.mark.parametrize("cg,M,N", [
+    (0, 1790, 2808),     # SM pairs: 7 x 11 = 77 tiles, one past a wave (rem 1, every tile split)
+    (0, 200, 38656),     # 1 x 151 = 151 tiles, rem 75 (one short of two waves)
+    (0, 768, 32504),     # 3 x 127 = 381 tiles, five waves + 1
+    (1, 1150, 4352),     # single SMs: 9 x 17 = 153 tiles, rem 1
+    (1, 384, 25856),     # 3 x 101 = 303 tiles, rem 151
+], ids=["pair_rem1", "pair_rem75", "pair_5waves_rem1", "cta1_rem1", "cta1_rem151"])
+def test_split_at_wave_boundaries(coda, cg, M, N, K):
+    """The split's edge cases on a GB300 with 76 SM pairs / 152 SMs: one tile
+    past a wave, one tile short of two waves, five whole waves before the
+    split, and the shortest reduction the split takes (16 k-blocks) with and
+    without a ragged last k-block. Against the data-parallel schedule within one
+    bf16 step, and repeatable."""
+    import torch
+    try:
+        coda.coda_set_cta_group(cg)
+        g = torch.Generator(device="cuda").manual_seed(M + N + K)
+        A = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+        B = (torch.randn(K, N, device="cuda", generator=g) * K ** -0.5).bfloat16()
+        dp, sk = _modes_raw(coda, lambda: coda.coda_gemm(A, B))
+    finally:
+        coda.coda_set_cta_group(0)
+    d = (sk.float() - dp.float()).abs()
+    step = (dp.float().abs() * 2.0 ** -7).clamp_min(1e-4)
+    assert bool((d <= step).all()), f"{M}x{N}x{K}: split and data-parallel differ by more than one bf16 step"
+    assert not torch.equal(sk, dp), "the split did not run"
+    assert coda.coda_device_status(clear=True) == 0
+
