@@ -250,3 +250,33 @@ def test_split_at_wave_boundaries(coda, cg, M, N, K):
     assert not torch.equal(sk, dp), "the split did not run"
     assert coda.coda_device_status(clear=True) == 0
 
+
+def test_workspace_follows_stream_handles(coda):
+    """Streams created and destroyed one after another (through the driver API):
+    each one's first split launch finds or creates the stream's workspace. A
+    destroyed stream's handle may come back for a new stream; the library then
+    waits for the old stream's launches before reusing the workspace. Every
+    launch must give the bits of the same split launch on torch's stream."""
+    import ctypes
+    import torch
+    cu = ctypes.CDLL("libcuda.so.1")
+    g = torch.Generator(device="cuda").manual_seed(3)
+    A = torch.randn(1800, 1096, device="cuda", generator=g).bfloat16()
+    B = (torch.randn(1096, 3400, device="cuda", generator=g) * 1096 ** -0.5).bfloat16()
+    try:
+        coda.coda_set_stream_k(2)
+        ref = coda.coda_gemm(A, B).clone()
+        torch.cuda.synchronize()
+        for _ in range(4):
+            h = ctypes.c_void_p()
+            assert cu.cuStreamCreate(ctypes.byref(h), 1) == 0  # CU_STREAM_NON_BLOCKING
+            s = torch.cuda.ExternalStream(h.value)
+            outs = [coda.coda_gemm(A, B, stream=s) for _ in range(2)]
+            s.synchronize()
+            for o in outs:
+                assert torch.equal(o, ref)
+            assert cu.cuStreamDestroy_v2(h) == 0
+    finally:
+        coda.coda_set_stream_k(1)
+    assert coda.coda_device_status(clear=True) == 0
+
