@@ -501,7 +501,10 @@ int coda_block_fwd(const coda_block_t* b, coda_stream_t stream);
  * CODA_ERR_UNSUPPORTED (M = 16384 fits up to d = 8192). Two calls whose
  * kernels can overlap on the GPU (calls on different streams, or from threads
  * whose streams are not ordered) race on that array and give undefined
- * results; calls on one stream run in order and are safe. Allocates nothing.
+ * results; calls on one stream run in order and are safe. Allocates nothing:
+ * its GEMMs never take the stream-K split (coda_set_stream_k), whose
+ * per-stream workspace would be allocated, so at sizes where coda_block_fwd
+ * splits, the two differ in fp32 accumulation order.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and keeps it for the process; make
  * that first call before any stream capture. */
