@@ -41,7 +41,9 @@
  *     detected on the host before anything is launched.
  *   - Kernels never trap. Each mbarrier wait inside them is bounded; a wait
  *     that runs out sets CODA_DEVST_TIMEOUT in the device status word and the
- *     kernel returns early. Out-of-range labels set CODA_DEVST_BAD_LABEL.
+ *     kernel returns early. Out-of-range labels set CODA_DEVST_BAD_LABEL. A
+ *     split tile whose arrival word could not be updated (see coda_set_stream_k)
+ *     sets CODA_DEVST_SPLIT and is left unwritten.
  *     Read (and clear) the word with coda_device_status().
  *   - A checked build of the same library (libcoda_checked.so, compiled with
  *     CODA_CHECKED=1) tests the index of every direct global load and store
