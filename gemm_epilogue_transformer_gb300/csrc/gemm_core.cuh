@@ -76,11 +76,11 @@ struct Cfg {
   // As many mainloop stages as the rest of shared memory leaves room for, at
   // most 6 (SM pair) or 4 (single SM).
   static constexpr int kFixedBytes = 1024 + kEpiWarps * kEpiWarpBytes + kInBytes + kShared + 16 +
-                                     8 * (2 + 2 + 1 + kEpiWarps * kMaxInSlots);
+                                     8 * (2 + 2 + 1 + kEpiWarps * kMaxInSlots + kEpiWarps * 8);
   static constexpr int kFitStages = (232448 - kFixedBytes) / (kStageBytes + 16);
   static constexpr int kMaxStages = kCG == 2 ? 6 : 4;
   static constexpr int kStages = kFitStages < kMaxStages ? kFitStages : kMaxStages;
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + kEpiWarps * kMaxInSlots + kEpiWarps * 8;
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + kEpiWarps * kEpiWarpBytes + kInBytes + kShared + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -512,6 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * C::kStages + 4);
   auto in_bar = [&](int ew_, int slot) { return smem_u32(bars + 2 * C::kStages + 5 + ew_ * kMaxInSlots + slot); };
+  // the last tile's input boxes, loaded all at once into the then idle mainloop
+  // stages: one barrier per chunk (at most 8) and epilogue warp
+  auto last_bar = [&](int ew_, int j) {
+    return smem_u32(bars + 2 * C::kStages + 5 + kEpiWarps * kMaxInSlots + ew_ * 8 + j);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -524,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     for (int i = 0; i < kEpiWarps * kMaxInSlots; ++i) mbar_init(in_bar(i / kMaxInSlots, i % kMaxInSlots), 1);
+    for (int i = 0; i < kEpiWarps * 8; ++i) mbar_init(last_bar(i / 8, i % 8), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -747,6 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto item_segs = [&](const Work& wk) { return wk.ncols / BSEG; };
     constexpr int kSegChunks = BSEG / 32;
+    // stage-memory bytes per epilogue warp for the last unit's inputs: 8 chunks
+    constexpr int kLastWarpBytes = 2 * kSegChunks * (kIn > 0 ? kIn : 1) * kInBoxBytes;
+    static_assert(kEpiWarps * kLastWarpBytes <= C::kStages * C::kStageBytes, "last unit's inputs fit the stages");
     int local = 0;
     int sbuf = 0;
     const int nslots = Epi::slots(ep);
@@ -757,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t in_base = smem_u32(s_in) + ew * InRingOf<Epi>::value;
     uint32_t seq_used = 0;    // chunks consumed (all lanes)
     uint32_t seq_issued = 0;  // chunks issued (lane 0)
+    int last_issued = 0;      // lane 0: chunks of the last unit loaded into the stage memory
     int it_s = 0, it_c = 0;  // issue cursor (lane 0): segment and chunk of work unit iw
     WorkCursor icur;
     work_begin(p, cluster_id, icur);
@@ -879,6 +889,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       // reopen at the 128-column segment boundary (chunk 4). A segment that
       // starts past N ends the item (only the last column block can).
       const int nchunks = item_segs(w) * kSegChunks;
+      // This CTA's last unit runs its epilogue exposed after the final MMA, and
+      // with a single input slot in the ring (the two-box epilogues at long K)
+      // each chunk would wait a full memory round trip. The mainloop stages are
+      // idle by then (every load has landed and every MMA completed), so the
+      // unit's input boxes not yet in the ring are all issued at once into
+      // them, one barrier per chunk. Measured: the SwiGLU backward at
+      // 4096x14336x4096 1.1 % faster; with a two-slot ring (K <= 3072) the same
+      // was 0.5 % slower, so rings of two or more slots keep the ring.
+      int in_idx = 0;           // input chunks of this unit consumed so far
+      int last_from = 1 << 30;  // first input chunk taken from the stage memory
+      const uint32_t last_base = s_base + static_cast<uint32_t>(ew * kLastWarpBytes);
+      if constexpr (kIn > 0 && C::kInSlots == 1) {
+        WorkCursor pc = ecur;
+        Work nx;
+        if (run && !work_next(p, cluster_id, num_clusters, pc, nx)) {
+          const int n_ring = __shfl_sync(0xffffffffu, static_cast<int>(seq_issued - seq_used), 0);
+          int n_in = 0;
+          for (int seg = 0; seg < item_segs(w); ++seg) {
+            EpiCtx sx;
+            if (!make_ctx(w, seg, sx)) break;
+            for (int cs = 0; cs < kSegChunks; ++cs) n_in += Epi::has_input(ep, sx, cs) ? 1 : 0;
+          }
+          if (n_in > n_ring) {
+            last_from = n_ring;
+            if (lane == 0) {
+              it_live = false;  // the ring issues nothing more
+              last_issued = n_in - n_ring;
+              int j = 0;
+              for (int seg = 0; seg < item_segs(w); ++seg) {
+                EpiCtx sx;
+                if (!make_ctx(w, seg, sx)) break;
+                for (int cs = 0; cs < kSegChunks; ++cs) {
+                  if (!Epi::has_input(ep, sx, cs)) continue;
+                  if (j >= n_ring) {
+                    const uint32_t dst = last_base + static_cast<uint32_t>((j - n_ring) * kIn * kInBoxBytes);
+                    const uint32_t bar = last_bar(ew, j - n_ring);
+                    mbar_arrive_expect_tx(bar, kIn * kInBoxBytes);
+#pragma unroll
+                    for (int b = 0; b < InLoadsOf<Epi>::value; ++b) {
+                      int map, x, y;
+                      Epi::in_coord(ep, sx, cs, b, map, x, y);
+                      tma_load_2d_hint(dst + b * kInBoxBytes, map ? &tmI1 : &tmI0, bar, x, y, pol_stream);
+                    }
+                  }
+                  ++j;
+                }
+              }
+            }
+          }
+        }
+      }
       if (run && make_ctx(w, 0, cx)) {
         typename Epi::State st;
         Epi::begin(st, ep, cx);
@@ -886,11 +947,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto do_chunk = [&](int c, const typename Epi::Pre& pre) {
           const int cs = c & (kSegChunks - 1);  // chunk index inside its segment
           uint32_t in = 0;
+          bool from_ring = false;
           if constexpr (kIn > 0) {
             if (Epi::has_input(ep, cx, cs)) {
-              const int slot = static_cast<int>(seq_used % C::kInSlots);
-              if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
-              in = in_base + slot * kIn * kInBoxBytes;
+              if (in_idx >= last_from) {
+                if (!wait_bounded(last_bar(ew, in_idx - last_from), 0u, p, abort_flag)) ok = false;
+                in = last_base + static_cast<uint32_t>((in_idx - last_from) * kIn * kInBoxBytes);
+              } else {
+                const int slot = static_cast<int>(seq_used % C::kInSlots);
+                if (!wait_bounded(in_bar(ew, slot), (seq_used / C::kInSlots) & 1u, p, abort_flag)) ok = false;
+                in = in_base + slot * kIn * kInBoxBytes;
+                from_ring = true;
+              }
+              ++in_idx;
             }
           }
           float acc[32];
@@ -946,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::kStageBufs == 2) sbuf ^= 1;
           }
           if constexpr (kIn > 0) {
-            if (in) {
+            if (from_ring) {
               ++seq_used;
               if (lane == 0) issue_ahead();
             }
@@ -982,9 +1051,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bulk_wait_all<0>();
       // input boxes still in flight (only after an abort) land before exit
-      if constexpr (kIn > 0)
+      if constexpr (kIn > 0) {
         for (uint32_t q = seq_used; q < seq_issued; ++q)
           wait_drain(in_bar(ew, static_cast<int>(q % C::kInSlots)), (q / C::kInSlots) & 1u, p.timeout_ns);
+        for (int j = 0; j < last_issued; ++j) wait_drain(last_bar(ew, j), 0u, p.timeout_ns);  // returns at once if waited
+      }
     }
     __syncwarp();
   }

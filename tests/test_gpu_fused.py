@@ -230,3 +230,46 @@ def test_ce_bad_label_sets_status(coda):
     t = f64(tgt)
     assert math.isnan(t[5]) and math.isnan(t[9])
     assert np.all(np.isfinite(np.delete(t, [5, 9])))
+
+
+def test_single_slot_input_ring_long_k(coda):
+    """K > 3072: the two-box input epilogues (SwiGLU backward with its GU
+    pre-activations; RMSNorm backward with the residual gradient) keep one chunk
+    of inputs in their ring, and each CTA's last tile takes its remaining input
+    boxes from the idle mainloop stages instead. Ragged shapes with more tiles
+    than one wave, both tile variants, with and without the stream-K split (whose
+    split pieces can be a CTA's last unit), against the oracle."""
+    import torch
+    M, F, K, d = 1800, 3400, 3208, 3400
+    p = gen.swiglu_problem(M, K, F, seed=61)
+    GU = gen.normal_bf16(np.random.default_rng(61), (M, 2 * F))
+    dY, Wd, gu = dev_bf16(p["dY"]), dev_bf16(p["Wd"]), dev_bf16(GU)
+    ref = O.gemm_swiglu_bwd(O.bf16(p["dY"]), O.bf16(p["Wd"]), O.bf16(GU))["dGU"]
+    R = np.random.default_rng(62)
+    dYr = gen.normal_bf16(R, (M, K))
+    W1 = gen.normal_bf16(R, (d, K), std=K ** -0.5)
+    h = gen.normal_bf16(R, (M, d))
+    gamma = gen.normal_bf16(R, (d,), std=0.1, mean=1.0)
+    dres = gen.normal_bf16(R, (M, d))
+    r = (R.random(M) + 0.5).astype(np.float32)
+    s = R.standard_normal(M).astype(np.float32)
+    rr = O.gemm_rmsnorm_bwd_res(O.bf16(dYr), O.bf16(W1), O.bf16(h), O.bf16(gamma), r.astype(np.float64),
+                                s.astype(np.float64), O.bf16(dres))
+    dr, ds = _dev_f32(r), _dev_f32(s)
+    try:
+        for cg in (0, 1):
+            for sk in (0, 2):
+                coda.coda_set_cta_group(cg)
+                coda.coda_set_stream_k(sk)
+                out = coda.coda_gemm_swiglu_bwd(dY, Wd, gu)
+                dh, pdg = coda.coda_gemm_rmsnorm_bwd_res(dev_bf16(dYr), dev_bf16(W1), dev_bf16(h), dev_bf16(gamma),
+                                                         dr, ds, dev_bf16(dres))
+                torch.cuda.synchronize()
+                assert_bf16(f64(out), ref, f"SwiGLU bwd dGU (cta group {cg}, split {sk})")
+                assert_bf16(f64(dh), rr["dh"], f"RMSNorm bwd + residual dh (cta group {cg}, split {sk})")
+                assert_stat(f64(coda.coda_colsum_reduce(pdg)), rr["dgamma"], f"dgamma (cta group {cg}, split {sk})")
+    finally:
+        coda.coda_set_cta_group(0)
+        coda.coda_set_stream_k(1)
+    assert coda.coda_device_status(clear=True) == 0
+
