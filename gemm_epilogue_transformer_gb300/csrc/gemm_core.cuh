@@ -198,10 +198,14 @@ struct Work {
 // from its first tile boundary [pos, end), then the piece before it [lo, hi):
 // every cluster then starts at k-block 0 of some tile and all of them move
 // through K in step, as in the data-parallel waves, so the operand slices
-// read at one time are few. Without it ([lo, end) in order) the clusters'
-// k positions are spread over the whole reduction, which is faster while the
-// stream-K tiles' operands fit in L2 together and much slower once they do
-// not.
+// read at one time are few. Without it the clusters' k positions are spread
+// over the whole reduction, which is faster while the stream-K tiles'
+// operands fit in L2 together and much slower once they do not; there each
+// cluster walks the shorter of its two parts [lo, b) and [b, end) (b the first
+// tile boundary) first. The longer part then covers the split epilogue of the
+// shorter one: the first whole tile after the range reuses the shorter
+// part's accumulator buffer, and a short second part would leave its MMAs
+// waiting for that epilogue.
 struct WorkCursor {
   int t, pos, end, lo, hi;
 };
@@ -271,7 +275,8 @@ __device__ __forceinline__ void work_begin(const GemmShape& p, int cluster, Work
   if (p.sk_tiles > 0) {
     w.lo = cluster * p.sk_q + (cluster < p.sk_r ? cluster : p.sk_r);
     w.end = w.lo + p.sk_q + (cluster < p.sk_r ? 1 : 0);
-    w.hi = p.sk_rotate ? (w.lo + p.k_blocks - 1) / p.k_blocks * p.k_blocks : w.lo;  // < end: range >= k_blocks
+    const int b = (w.lo + p.k_blocks - 1) / p.k_blocks * p.k_blocks;  // < end: range >= k_blocks
+    w.hi = (p.sk_rotate || w.end - b < b - w.lo) ? b : w.lo;
     w.pos = w.hi;
   }
 }
