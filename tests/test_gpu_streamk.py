@@ -280,3 +280,31 @@ def test_workspace_follows_stream_handles(coda):
         coda.coda_set_stream_k(1)
     assert coda.coda_device_status(clear=True) == 0
 
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (2048, 2552, 16376),   # 8 x 10 = 80 tiles, rem 4: every range is a tail piece and a head piece
+    (2048, 4344, 16376),   # 8 x 17 = 136 tiles, rem 60: ranges of 1.8 tiles (tail, whole tile, head)
+], ids=["rem4", "rem60"])
+def test_split_rotated_walk(coda, M, N, K):
+    """Long reductions whose split tiles' operands exceed half of L2 (eight row
+    blocks and ten or more column blocks of 256 over K = 16376: 151-210 MB), so each
+    cluster walks its range from its first tile boundary and takes the piece
+    before it last, as the long-K dX GEMM does; B is K-major as there. Against
+    the data-parallel schedule within one bf16 step, repeatable, and sampled
+    rows and columns against the float64 oracle."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(N + K)
+    A = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+    B = (torch.randn(N, K, device="cuda", generator=g) * K ** -0.5).bfloat16()
+    dp, sk = _modes_raw(coda, lambda: coda.coda_gemm(A, B, transB=True))
+    d = (sk.float() - dp.float()).abs()
+    step = (dp.float().abs() * 2.0 ** -7).clamp_min(1e-4)
+    assert bool((d <= step).all()), f"{M}x{N}x{K}: split and data-parallel differ by more than one bf16 step"
+    assert not torch.equal(sk, dp), "the split did not run"
+    rng = np.random.default_rng(N)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, 30, replace=False)]))
+    cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 30, replace=False)]))
+    ref = O.matmul(f64(A[rows]), f64(B[cols]).T)
+    assert_bf16(f64(sk[rows][:, cols]), ref, "split GEMM, sampled rows and columns")
+    assert coda.coda_device_status(clear=True) == 0
