@@ -4,6 +4,8 @@
 // grid-stride loops sized to the SM count, fp32 arithmetic, bf16 storage.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "host.h"
 
 using namespace coda;
@@ -48,12 +50,35 @@ __device__ float block_sum(float v, float* sh) {
   return v;
 }
 
+// Blocks for a one-item-per-step grid-stride kernel: up to 8 per SM (2048
+// threads of 256).
 int grid_for(const DeviceInfo* di, long work_items, int block) {
   long g = (work_items + block - 1) / block;
   const long cap = static_cast<long>(di->sm_count) * 8;
   if (g < 1) g = 1;
   return static_cast<int>(g < cap ? g : cap);
 }
+
+// Blocks for a grid-stride kernel: as many as the SMs hold at once (the SM
+// count times the kernel's occupancy, queried once per call site into
+// per_sm), so every block runs from the start and the equal per-thread shares
+// end together; fewer when the work is smaller.
+template <class Kern>
+int grid_resident(const DeviceInfo* di, Kern kernel, std::atomic<int>& per_sm, long work_items, int block) {
+  int n = per_sm.load();
+  if (n <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, 0) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 2;
+    }
+    per_sm.store(n);
+  }
+  long g = (work_items + block - 1) / block;
+  const long cap = static_cast<long>(di->sm_count) * n;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < cap ? g : cap);
+}
+
 int launched(const char* fn) {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CODA_OK : fail_cuda(e, fn);
@@ -62,42 +87,104 @@ int launched(const char* fn) {
 #define GRID_STRIDE(i, n) \
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < (n); i += static_cast<long>(gridDim.x) * blockDim.x)
 
+// Grid-stride over n items, kUnroll per step: a thread takes items i0 + j *
+// stride (j < kUnroll) and issues the loads of all of them before it computes
+// or stores any, so each thread has kUnroll 16-byte loads (per input) in
+// flight instead of one. Per element the arithmetic is the same as one item
+// at a time.
+constexpr int kUnroll = 4;
+#define GRID_STRIDE_STEP(i0, stride, n)                                 \
+  const long stride = static_cast<long>(gridDim.x) * blockDim.x;        \
+  for (long i0 = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i0 < (n); i0 += stride * kUnroll)
+
 __global__ void add_kernel(long nvec, const uint4* a, const uint4* b, uint4* out) {
-  GRID_STRIDE(i, nvec) {
-    float x[8], y[8];
-    unpack8(__ldg(a + i), x);
-    unpack8(__ldg(b + i), y);
+  GRID_STRIDE_STEP(i0, stride, nvec) {
+    uint4 ra[kUnroll], rb[kUnroll];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] += y[k];
-    out[i] = pack8(x);
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nvec) {
+        ra[j] = __ldg(a + i);
+        rb[j] = __ldg(b + i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nvec) {
+        float x[8], y[8];
+        unpack8(ra[j], x);
+        unpack8(rb[j], y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] += y[k];
+        out[i] = pack8(x);
+      }
+    }
   }
 }
 
-// One block per row (grid-stride over rows): r = 1/sqrt(mean h^2 + eps), n = r h gamma.
+// One block per row (grid-stride over rows): r = 1/sqrt(mean h^2 + eps),
+// n = r h gamma. With kVec > 0 (d <= 8 * kVec * blockDim) a thread keeps its
+// kVec vectors of the row in registers between the two passes, all loaded at
+// once; with kVec = 0 it loops over the row twice (any width).
+template <int kVec>
 __global__ void rmsnorm_kernel(int M, int d, const __nv_bfloat16* h, const __nv_bfloat16* gamma, float eps,
                                __nv_bfloat16* n, float* r_out) {
   __shared__ float sh[32];
   const int nv = d / 8;
   for (int row = blockIdx.x; row < M; row += gridDim.x) {
     const __nv_bfloat16* hr = h + static_cast<long>(row) * d;
-    float ss = 0.f;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float x[8];
-      unpack8(ld16(hr + 8 * v), x);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
-    }
-    ss = block_sum(ss, sh);
-    const float r = 1.0f / sqrtf(ss / d + eps);
-    if (threadIdx.x == 0 && r_out) r_out[row] = r;
     __nv_bfloat16* nr = n + static_cast<long>(row) * d;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float x[8], g[8];
-      unpack8(ld16(hr + 8 * v), x);
-      unpack8(ld16(gamma + 8 * v), g);
+    float ss = 0.f;
+    if constexpr (kVec > 0) {
+      uint4 raw[kVec];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = (x[k] * r) * g[k];
-      st16(nr + 8 * v, pack8(x));
+      for (int j = 0; j < kVec; ++j) {
+        const int v = threadIdx.x + j * blockDim.x;
+        if (v < nv) raw[j] = ld16(hr + 8 * v);
+      }
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        if (threadIdx.x + j * blockDim.x < nv) {
+          float x[8];
+          unpack8(raw[j], x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
+        }
+      }
+      ss = block_sum(ss, sh);
+      const float r = 1.0f / sqrtf(ss / d + eps);
+      if (threadIdx.x == 0 && r_out) r_out[row] = r;
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        const int v = threadIdx.x + j * blockDim.x;
+        if (v < nv) {
+          float x[8], g[8];
+          unpack8(raw[j], x);
+          unpack8(ld16(gamma + 8 * v), g);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[k] = (x[k] * r) * g[k];
+          st16(nr + 8 * v, pack8(x));
+        }
+      }
+    } else {
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float x[8];
+        unpack8(ld16(hr + 8 * v), x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
+      }
+      ss = block_sum(ss, sh);
+      const float r = 1.0f / sqrtf(ss / d + eps);
+      if (threadIdx.x == 0 && r_out) r_out[row] = r;
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float x[8], g[8];
+        unpack8(ld16(hr + 8 * v), x);
+        unpack8(ld16(gamma + 8 * v), g);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = (x[k] * r) * g[k];
+        st16(nr + 8 * v, pack8(x));
+      }
     }
   }
 }
@@ -116,36 +203,67 @@ __global__ void rowscale_kernel(int M, int N, const __nv_bfloat16* x, const floa
 
 // Each item: 8 outputs from 16 interleaved gate/up values.
 __global__ void swiglu_kernel(long nitems, const __nv_bfloat16* gu, __nv_bfloat16* a) {
-  GRID_STRIDE(i, nitems) {
-    float p[8], q[8], o[8];
-    unpack8(ld16(gu + 16 * i), p);
-    unpack8(ld16(gu + 16 * i + 8), q);
+  GRID_STRIDE_STEP(i0, stride, nitems) {
+    uint4 rp[kUnroll], rq[kUnroll];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      o[k] = p[2 * k] / (1.0f + exp_f(-p[2 * k])) * p[2 * k + 1];
-      o[k + 4] = q[2 * k] / (1.0f + exp_f(-q[2 * k])) * q[2 * k + 1];
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nitems) {
+        rp[j] = ld16(gu + 16 * i);
+        rq[j] = ld16(gu + 16 * i + 8);
+      }
     }
-    st16(a + 8 * i, pack8(o));
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nitems) {
+        float p[8], q[8], o[8];
+        unpack8(rp[j], p);
+        unpack8(rq[j], q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          o[k] = p[2 * k] / (1.0f + exp_f(-p[2 * k])) * p[2 * k + 1];
+          o[k + 4] = q[2 * k] / (1.0f + exp_f(-q[2 * k])) * q[2 * k + 1];
+        }
+        st16(a + 8 * i, pack8(o));
+      }
+    }
   }
 }
 
 __global__ void swiglu_bwd_kernel(long nitems, const __nv_bfloat16* dA, const __nv_bfloat16* gu,
                                   __nv_bfloat16* dgu) {
-  GRID_STRIDE(i, nitems) {
-    float da[8];
-    unpack8(ld16(dA + 8 * i), da);
+  GRID_STRIDE_STEP(i0, stride, nitems) {
+    uint4 rd[kUnroll], rg[kUnroll][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float g[8], o[8];
-      unpack8(ld16(gu + 16 * i + 8 * h), g);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float G = g[2 * k], U = g[2 * k + 1], d = da[4 * h + k];
-        const float s = 1.0f / (1.0f + exp_f(-G));
-        o[2 * k] = d * U * s * (1.0f + G * (1.0f - s));
-        o[2 * k + 1] = d * G * s;
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nitems) {
+        rd[j] = ld16(dA + 8 * i);
+        rg[j][0] = ld16(gu + 16 * i);
+        rg[j][1] = ld16(gu + 16 * i + 8);
       }
-      st16(dgu + 16 * i + 8 * h, pack8(o));
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const long i = i0 + j * stride;
+      if (i < nitems) {
+        float da[8];
+        unpack8(rd[j], da);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float g[8], o[8];
+          unpack8(rg[j][h], g);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float G = g[2 * k], U = g[2 * k + 1], d = da[4 * h + k];
+            const float s = 1.0f / (1.0f + exp_f(-G));
+            o[2 * k] = d * U * s * (1.0f + G * (1.0f - s));
+            o[2 * k + 1] = d * G * s;
+          }
+          st16(dgu + 16 * i + 8 * h, pack8(o));
+        }
+      }
     }
   }
 }
@@ -178,39 +296,61 @@ __global__ void rope_kernel(int M, int N, const float* ct, const float* st, int 
   }
 }
 
-// One block per row: online max / sum-exp, argmax (lowest index), target.
+// One warp per row (grid-stride over rows): online max / sum-exp, argmax
+// (lowest index), target. Each lane loads kCeBatch 16-byte vectors of the row
+// before it uses any of them, so a warp keeps 4 KiB in flight, and rescales its
+// running sum once per batch of 64 values.
+constexpr int kCeBatch = 8;
 __global__ void ce_fwd_kernel(int M, int V, const __nv_bfloat16* logits, const int32_t* labels, float* lse_out,
                               float* loss_row, int32_t* argmax_out, int* status) {
-  __shared__ float sm[32], ss[32];
-  __shared__ int si[32];
+  const int lane = threadIdx.x & 31;
   const int nv = V / 8;
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int row = blockIdx.x; row < M; row += gridDim.x) {
-    const __nv_bfloat16* lr = logits + static_cast<long>(row) * V;
+  const long nwarps = static_cast<long>(gridDim.x) * (blockDim.x >> 5);
+  for (long row = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < M;
+       row += nwarps) {
+    const __nv_bfloat16* lr = logits + row * V;
     float m = -INFINITY, s = 0.f;
     int bi = 0x7fffffff;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float x[8];
-      unpack8(ld16(lr + 8 * v), x);
-      float cm = x[0];
-      int ci = 0;
+    for (int v0 = lane; v0 < nv; v0 += 32 * kCeBatch) {
+      uint4 raw[kCeBatch];
 #pragma unroll
-      for (int k = 1; k < 8; ++k)
-        if (x[k] > cm) {
-          cm = x[k];
-          ci = k;
-        }
-      if (cm > m) {
-        bi = 8 * v + ci;
+      for (int j = 0; j < kCeBatch; ++j) {
+        const int v = v0 + 32 * j;
+        raw[j] = v < nv ? ld16(lr + 8L * v) : make_uint4(0, 0, 0, 0);
       }
+      // batch maximum; vectors and their elements in increasing column order,
+      // so the first occurrence of the maximum is kept
+      float cm = -INFINITY;
+      int ci = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < kCeBatch; ++j) {
+        if (v0 + 32 * j < nv) {
+          float x[8];
+          unpack8(raw[j], x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (x[k] > cm) {
+              cm = x[k];
+              ci = 8 * (v0 + 32 * j) + k;
+            }
+        }
+      }
+      if (cm > m) bi = ci;
       const float nm = fmaxf(m, cm);
       float add = 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) add += exp_f(x[k] - nm);
+      for (int j = 0; j < kCeBatch; ++j) {
+        if (v0 + 32 * j < nv) {
+          float x[8];
+          unpack8(raw[j], x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) add += exp_f(x[k] - nm);
+        }
+      }
       s = s * exp_f(m - nm) + add;
       m = nm;
     }
-    // warp combine (m, s, bi)
+    // warp combine (m, s, bi); a lane that saw no column has m = -inf, s = 0
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -223,24 +363,8 @@ __global__ void ce_fwd_kernel(int M, int V, const __nv_bfloat16* logits, const i
       s = a1 + a2;
       m = nm;
     }
-    if (l == 0) {
-      sm[w] = m;
-      ss[w] = s;
-      si[w] = bi;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float M_ = sm[0], S_ = ss[0];
-      int B_ = si[0];
-      for (int k = 1; k < nw; ++k) {
-        const float nm = fmaxf(M_, sm[k]);
-        const float a1 = (M_ == -INFINITY) ? 0.f : S_ * exp_f(M_ - nm);
-        const float a2 = (sm[k] == -INFINITY) ? 0.f : ss[k] * exp_f(sm[k] - nm);
-        if (sm[k] > M_ || (sm[k] == M_ && si[k] < B_)) B_ = si[k];
-        S_ = a1 + a2;
-        M_ = nm;
-      }
-      const float lse = M_ + logf(S_);
+    if (lane == 0) {
+      const float lse = m + logf(s);
       const int y = labels[row];
       float t;
       if (y < 0 || y >= V) {
@@ -251,9 +375,8 @@ __global__ void ce_fwd_kernel(int M, int V, const __nv_bfloat16* logits, const i
       }
       lse_out[row] = lse;
       loss_row[row] = lse - t;
-      if (argmax_out) argmax_out[row] = B_;
+      if (argmax_out) argmax_out[row] = bi;
     }
-    __syncthreads();
   }
 }
 
@@ -311,9 +434,126 @@ __global__ void rowdot_kernel(int M, int N, float inv_d, const __nv_bfloat16* dY
   }
 }
 
-// One block per 32-row tile: per row c = (1/d) sum G gamma h (block reduce),
-// dh = r gamma G - r^3 c h; column partials of r G h kept in shared memory.
-__global__ void rmsnorm_bwd_kernel(int M, int d, const __nv_bfloat16* G, const __nv_bfloat16* h,
+// One block of kRbThreads per 32-row tile (the partials' row blocks), its rows
+// in four groups of kRbGroup. For a group, two warps per row form
+// c = (1/d) sum G gamma h with kRowBatch vectors of G and of h in flight per
+// thread; then each thread takes its kOwn column vectors through the group's
+// rows, kPair2 at a time (read back from L2, where phase one just brought them),
+// writing dh = r gamma G - r^3 c h and accumulating the column partials of
+// r G h in registers. Covers d <= 8 * kRbThreads * kOwn.
+constexpr int kRbThreads = 512;
+constexpr int kRbGroup = 8;
+constexpr int kRowBatch = 4;
+template <int kOwn, int kPair2 = (kOwn >= 4 ? 1 : 2)>
+__global__ void __launch_bounds__(kRbThreads) rmsnorm_bwd_kernel(int M, int d, const __nv_bfloat16* G,
+                                                                 const __nv_bfloat16* h,
+                                                                 const __nv_bfloat16* gamma, const float* r,
+                                                                 __nv_bfloat16* dh, float* pdg) {
+  __shared__ float part[2][kRbGroup][2];
+  const int nv = d / 8;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grow = w >> 1;              // the group row this warp reduces
+  const int q = ((w & 1) << 5) | lane;  // this thread's place among the row's 64
+  const int r0 = blockIdx.x * 32;
+  float acc[kOwn][8];
+#pragma unroll
+  for (int o = 0; o < kOwn; ++o)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[o][k] = 0.f;
+#pragma unroll 1
+  for (int g = 0; g < 32 / kRbGroup; ++g) {
+    const int gr0 = r0 + g * kRbGroup;
+    if (gr0 >= M) break;  // the same for every thread of the block
+    // phase one: the group's row statistics
+    const int row = gr0 + grow;
+    float c = 0.f;
+    if (row < M) {
+      const long off = static_cast<long>(row) * d;
+      for (int v0 = q; v0 < nv; v0 += 64 * kRowBatch) {
+        uint4 ga[kRowBatch], ha[kRowBatch];
+#pragma unroll
+        for (int j = 0; j < kRowBatch; ++j) {
+          const int v = v0 + 64 * j;
+          if (v < nv) {
+            ga[j] = ld16(G + off + 8L * v);
+            ha[j] = ld16(h + off + 8L * v);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kRowBatch; ++j) {
+          const int v = v0 + 64 * j;
+          if (v < nv) {
+            float a[8], b[8], gg[8];
+            unpack8(ga[j], a);
+            unpack8(ha[j], b);
+            unpack8(ld16(gamma + 8 * v), gg);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) c = fmaf(a[k] * gg[k], b[k], c);
+          }
+        }
+      }
+    }
+    c = warp_sum(c);
+    if (lane == 0) part[g & 1][grow][w & 1] = c;
+    __syncthreads();
+    // phase two: gradients and column partials, kPair2 rows at a time
+#pragma unroll 1
+    for (int i = 0; i < kRbGroup; i += kPair2) {
+      const int ra = gr0 + i;
+      if (ra >= M) break;
+      const int nrows = ra + kPair2 <= M ? kPair2 : M - ra;
+      uint4 ga[kPair2][kOwn], ha[kPair2][kOwn];
+#pragma unroll
+      for (int t = 0; t < kPair2; ++t)
+#pragma unroll
+        for (int o = 0; o < kOwn; ++o) {
+          const int v = threadIdx.x + kRbThreads * o;
+          if (t < nrows && v < nv) {
+            const long off = static_cast<long>(ra + t) * d + 8L * v;
+            ga[t][o] = ld16(G + off);
+            ha[t][o] = ld16(h + off);
+          }
+        }
+#pragma unroll
+      for (int t = 0; t < kPair2; ++t) {
+        if (t >= nrows) break;
+        const float cr = (part[g & 1][i + t][0] + part[g & 1][i + t][1]) / d;
+        const float rv = r[ra + t];
+        const float r3c = rv * rv * rv * cr;
+#pragma unroll
+        for (int o = 0; o < kOwn; ++o) {
+          const int v = threadIdx.x + kRbThreads * o;
+          if (v < nv) {
+            float a[8], b[8], gg[8], out[8];
+            unpack8(ga[t][o], a);
+            unpack8(ha[t][o], b);
+            unpack8(ld16(gamma + 8 * v), gg);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              out[k] = rv * gg[k] * a[k] - r3c * b[k];
+              acc[o][k] += rv * a[k] * b[k];
+            }
+            st16(dh + static_cast<long>(ra + t) * d + 8L * v, pack8(out));
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 0; o < kOwn; ++o) {
+    const int v = threadIdx.x + kRbThreads * o;
+    if (v < nv) {
+      float4* dst = reinterpret_cast<float4*>(pdg + static_cast<long>(blockIdx.x) * d + 8L * v);
+      dst[0] = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+      dst[1] = make_float4(acc[o][4], acc[o][5], acc[o][6], acc[o][7]);
+    }
+  }
+}
+
+// Wider rows (d > 8 * kRbThreads * 4): one block per 32-row tile, one row at
+// a time: per row c = (1/d) sum G gamma h (block reduce), dh = r gamma G -
+// r^3 c h; column partials of r G h kept in shared memory.
+__global__ void rmsnorm_bwd_wide_kernel(int M, int d, const __nv_bfloat16* G, const __nv_bfloat16* h,
                                    const __nv_bfloat16* gamma, const float* r, __nv_bfloat16* dh, float* pdg) {
   extern __shared__ float colacc[];
   __shared__ float sh[32];
@@ -375,7 +615,8 @@ int coda_unfused_add(int M, int N, const coda_bf16* a, const coda_bf16* b, coda_
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const long nvec = static_cast<long>(M) * N / 8;
-  add_kernel<<<grid_for(di, nvec, 256), 256, 0, as_stream(stream)>>>(nvec, reinterpret_cast<const uint4*>(a),
+  static std::atomic<int> occ{0};
+  add_kernel<<<grid_resident(di, add_kernel, occ, nvec, 256), 256, 0, as_stream(stream)>>>(nvec, reinterpret_cast<const uint4*>(a),
                                                                      reinterpret_cast<const uint4*>(b),
                                                                      reinterpret_cast<uint4*>(out));
   return launched(fn);
@@ -394,9 +635,13 @@ int coda_unfused_rmsnorm(int M, int d, const coda_bf16* h, const coda_bf16* gamm
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const int grid = M < di->sm_count * 16 ? M : di->sm_count * 16;
-  rmsnorm_kernel<<<grid, 256, 0, as_stream(stream)>>>(M, d, reinterpret_cast<const __nv_bfloat16*>(h),
-                                                      reinterpret_cast<const __nv_bfloat16*>(gamma), eps,
-                                                      reinterpret_cast<__nv_bfloat16*>(n_out), r_out);
+  const auto* hb = reinterpret_cast<const __nv_bfloat16*>(h);
+  const auto* gb = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  auto* nb = reinterpret_cast<__nv_bfloat16*>(n_out);
+  if (d / 8 <= 4 * 256)
+    rmsnorm_kernel<4><<<grid, 256, 0, as_stream(stream)>>>(M, d, hb, gb, eps, nb, r_out);
+  else
+    rmsnorm_kernel<0><<<grid, 256, 0, as_stream(stream)>>>(M, d, hb, gb, eps, nb, r_out);
   return launched(fn);
 }
 
@@ -423,7 +668,8 @@ int coda_unfused_swiglu(int M, int F, const coda_bf16* gu, coda_bf16* A_out, cod
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const long n = static_cast<long>(M) * F / 8;
-  swiglu_kernel<<<grid_for(di, n, 256), 256, 0, as_stream(stream)>>>(n, reinterpret_cast<const __nv_bfloat16*>(gu),
+  static std::atomic<int> occ{0};
+  swiglu_kernel<<<grid_resident(di, swiglu_kernel, occ, n, 256), 256, 0, as_stream(stream)>>>(n, reinterpret_cast<const __nv_bfloat16*>(gu),
                                                                      reinterpret_cast<__nv_bfloat16*>(A_out));
   return launched(fn);
 }
@@ -439,7 +685,8 @@ int coda_unfused_swiglu_bwd(int M, int F, const coda_bf16* dA, const coda_bf16* 
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
   const long n = static_cast<long>(M) * F / 8;
-  swiglu_bwd_kernel<<<grid_for(di, n, 256), 256, 0, as_stream(stream)>>>(
+  static std::atomic<int> occ{0};
+  swiglu_bwd_kernel<<<grid_resident(di, swiglu_bwd_kernel, occ, n, 256), 256, 0, as_stream(stream)>>>(
       n, reinterpret_cast<const __nv_bfloat16*>(dA), reinterpret_cast<const __nv_bfloat16*>(gu),
       reinterpret_cast<__nv_bfloat16*>(dgu_out));
   return launched(fn);
@@ -492,9 +739,11 @@ int coda_unfused_ce_fwd(int M, int V, const coda_bf16* logits, const int32_t* la
   CODA_REQ_OPT4(argmax_out);
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
-  const int grid = M < di->sm_count * 16 ? M : di->sm_count * 16;
+  // one warp per row, 8 warps per block
+  const long blocks = (static_cast<long>(M) + 7) / 8;
+  const int grid = static_cast<int>(blocks < di->sm_count * 16L ? blocks : di->sm_count * 16L);
   cudaStream_t st = as_stream(stream);
-  ce_fwd_kernel<<<grid, 512, 0, st>>>(M, V, reinterpret_cast<const __nv_bfloat16*>(logits), labels, lse_out,
+  ce_fwd_kernel<<<grid, 256, 0, st>>>(M, V, reinterpret_cast<const __nv_bfloat16*>(logits), labels, lse_out,
                                       loss_row_out, argmax_out, di->status);
   rc = launched(fn);
   if (rc || !loss_mean_out) return rc;
@@ -550,16 +799,28 @@ int coda_unfused_rmsnorm_bwd(int M, int d, const coda_bf16* G, const coda_bf16* 
   CODA_REQ_PTR4(pdg_out);
   const DeviceInfo* di = current_device();
   if (!di) return CODA_ERR_UNSUPPORTED;
-  const size_t smem = static_cast<size_t>(d) * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&rmsnorm_bwd_kernel),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(rmsnorm_bwd)");
-  }
   const int tiles = (M + 31) / 32;
-  rmsnorm_bwd_kernel<<<tiles, 512, smem, as_stream(stream)>>>(
-      M, d, reinterpret_cast<const __nv_bfloat16*>(G), reinterpret_cast<const __nv_bfloat16*>(h),
-      reinterpret_cast<const __nv_bfloat16*>(gamma), r, reinterpret_cast<__nv_bfloat16*>(dh_out), pdg_out);
+  const auto* Gb = reinterpret_cast<const __nv_bfloat16*>(G);
+  const auto* hb = reinterpret_cast<const __nv_bfloat16*>(h);
+  const auto* gb = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  auto* db = reinterpret_cast<__nv_bfloat16*>(dh_out);
+  cudaStream_t st = as_stream(stream);
+  const int nv = d / 8;
+  if (nv <= kRbThreads) {
+    rmsnorm_bwd_kernel<1><<<tiles, kRbThreads, 0, st>>>(M, d, Gb, hb, gb, r, db, pdg_out);
+  } else if (nv <= 2 * kRbThreads) {
+    rmsnorm_bwd_kernel<2><<<tiles, kRbThreads, 0, st>>>(M, d, Gb, hb, gb, r, db, pdg_out);
+  } else if (nv <= 4 * kRbThreads) {
+    rmsnorm_bwd_kernel<4><<<tiles, kRbThreads, 0, st>>>(M, d, Gb, hb, gb, r, db, pdg_out);
+  } else {
+    const size_t smem = static_cast<size_t>(d) * sizeof(float);
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&rmsnorm_bwd_wide_kernel),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(rmsnorm_bwd)");
+    }
+    rmsnorm_bwd_wide_kernel<<<tiles, 512, smem, st>>>(M, d, Gb, hb, gb, r, db, pdg_out);
+  }
   return launched(fn);
 }
 

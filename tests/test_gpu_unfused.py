@@ -26,7 +26,7 @@ def test_add_rowscale(coda, M, N):
     assert_bf16(f64(s), f64(r)[:, None] * O.bf16(a), "rowscale")
 
 
-@pytest.mark.parametrize("M,d", [(300, 520), (64, 8192), (3, 8)])
+@pytest.mark.parametrize("M,d", [(300, 520), (64, 8192), (3, 8), (33, 16384), (40, 20480)])
 def test_rmsnorm_fwd_bwd(coda, M, d):
     h = gen.normal_bf16(_rng(4), (M, d))
     g = gen.normal_bf16(_rng(5), (d,), std=0.1, mean=1.0)
@@ -76,7 +76,7 @@ def test_rope(coda, M, N, hd, rope_cols, S):
     assert_bf16(f64(t), O.rope_bwd(O.bf16(x), pos, hd, 10000.0, rope_cols), "rope bwd")
 
 
-@pytest.mark.parametrize("M,V", [(300, 1000), (4, 32768), (2, 8)])
+@pytest.mark.parametrize("M,V", [(300, 1000), (4, 32768), (2, 8), (13, 4104)])
 def test_ce(coda, M, V):
     import torch
     L = gen.normal_bf16(_rng(10), (M, V), std=3.0)
