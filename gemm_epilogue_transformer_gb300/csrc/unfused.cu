@@ -539,13 +539,14 @@ __global__ void __launch_bounds__(kRbThreads) rmsnorm_bwd_kernel(int M, int d, c
       }
     }
   }
+  // scalar stores: the partials need only 4-byte alignment
 #pragma unroll
   for (int o = 0; o < kOwn; ++o) {
     const int v = threadIdx.x + kRbThreads * o;
     if (v < nv) {
-      float4* dst = reinterpret_cast<float4*>(pdg + static_cast<long>(blockIdx.x) * d + 8L * v);
-      dst[0] = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
-      dst[1] = make_float4(acc[o][4], acc[o][5], acc[o][6], acc[o][7]);
+      float* dst = pdg + static_cast<long>(blockIdx.x) * d + 8L * v;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dst[k] = acc[o][k];
     }
   }
 }

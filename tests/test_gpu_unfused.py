@@ -90,3 +90,26 @@ def test_ce(coda, M, V):
     assert np.array_equal(am.cpu().numpy(), ref["argmax"])
     dl = coda.coda_unfused_ce_bwd(dev_bf16(L), torch.from_numpy(y).cuda(), lse, 1.0 / M)
     assert_bf16(f64(dl), O.ce_bwd(O.bf16(L), y, f64(lse), 1.0 / M), "dl")
+
+
+@pytest.mark.parametrize("M,d", [(40, 520), (33, 8192)])
+def test_rmsnorm_bwd_partials_4byte_aligned(coda, M, d):
+    """The dgamma partials may start on any 4-byte boundary (the entry point
+    checks 4-byte alignment only): results bitwise equal to an aligned call."""
+    import torch
+    h = dev_bf16(gen.normal_bf16(_rng(12), (M, d)))
+    g = dev_bf16(gen.normal_bf16(_rng(13), (d,), std=0.1, mean=1.0))
+    G = dev_bf16(gen.normal_bf16(_rng(14), (M, d)))
+    _, r = coda.coda_unfused_rmsnorm(h, g, 1e-6)
+    dh_ref, pdg_ref = coda.coda_unfused_rmsnorm_bwd(G, h, g, r)
+    rows = coda.coda_num_row_tiles(M)
+    buf = torch.full((rows * d + 1,), float("nan"), dtype=torch.float32, device=G.device)
+    pdg = buf[1:].view(rows, d)  # 4 bytes past a 256-byte boundary
+    assert pdg.data_ptr() % 16 == 4
+    dh = torch.empty_like(G)
+    rc = coda.lib().coda_unfused_rmsnorm_bwd(M, d, G.data_ptr(), h.data_ptr(), g.data_ptr(), r.data_ptr(),
+                                            dh.data_ptr(), pdg.data_ptr(), None)
+    assert rc == 0, coda.lib().coda_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(dh, dh_ref)
+    assert torch.equal(pdg, pdg_ref)
