@@ -143,7 +143,10 @@ int check_block(const char* fn, const coda_block_t* b) {
   return CODA_OK;
 }
 
-// Scratch of coda_block_fwd_noalloc: the forward's only scratch, the
+// Scratch of coda_block_fwd_noalloc, the forward for callers that cannot
+// allocate device memory (a plugin given only its input and output buffers, a
+// serving loop that may not call cudaMalloc after start-up, a process whose
+// pool holds the device's memory): the forward's only scratch, the
 // per-(row, 128-column block) sum-of-squares partials, in a file-scope device
 // array instead of the caller's workspace. One array per device (the module
 // is loaded per context), shared by every call on that device.

@@ -495,8 +495,12 @@ size_t coda_block_workspace_bytes(int M, int d, int F, int unfused);
 int coda_block_fwd(const coda_block_t* b, coda_stream_t stream);
 
 /* coda_block_fwd_noalloc: the fused forward for callers that cannot allocate
- * device memory. It has no counterpart on the pages (a deployment convenience
- * of this library). It runs the launch sequence of coda_block_fwd but ignores
+ * device memory: a plugin that its host engine hands only input and output
+ * buffers, with no allocator and no workspace; a serving loop that may not
+ * call cudaMalloc after start-up, because the call can synchronise the device
+ * and take an unbounded time; a process whose memory pool already holds the
+ * device's memory. It has no counterpart on the pages (a deployment
+ * convenience of this library). It runs the launch sequence of coda_block_fwd but ignores
  * b->workspace: the forward's only scratch, the sum-of-squares partials
  * (M * ceil(d/128) fp32 values), lives in a 4 MiB file-scope device array of
  * the library, one per device. Sizes with M * ceil(d/128) * 4 > 4 MiB return

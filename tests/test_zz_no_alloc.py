@@ -1,8 +1,11 @@
-"""The block-chain forward without a caller workspace (coda_block_fwd_noalloc):
-its sum-of-squares partials live in the library's static device array. Two
-calls in a row on one stream must both give the workspace variant's bits and
-match the float64 oracle; a size past the array's limit is refused before any
-launch."""
+"""The block-chain forward without a caller workspace (coda_block_fwd_noalloc),
+for callers that cannot allocate device memory: a plugin given only its input
+and output buffers, a serving loop that may not call cudaMalloc after start-up
+(the call can synchronise the device and take unbounded time), a process whose
+pool already holds the device's memory. Its sum-of-squares partials live in
+the library's static device array. Two calls in a row on one stream must both
+give the workspace variant's bits and match the float64 oracle; a size past
+the array's limit is refused before any launch."""
 import numpy as np
 import pytest
 
