@@ -171,6 +171,22 @@ def test_block_chain_host_validation(lib):
     assert lib.coda_rope_bwd_rowdot(8, 96, good, good, good, good, good, 16, 16, 48, 0, good, good, None) == INVALID
 
 
+def test_block_fwd_noalloc_host_validation(lib):
+    """The allocation-free forward refuses a null descriptor, negative sizes and
+    partials past its static array before it looks up any device address."""
+    INVALID, UNSUPPORTED = -1, -2
+    from gemm_epilogue_transformer_gb300 import _lib
+    assert lib.coda_block_fwd_noalloc(None, None) == INVALID
+    b = _lib.CodaBlock()
+    b.M, b.d, b.F = -1, 64, 64
+    assert lib.coda_block_fwd_noalloc(b, None) == INVALID
+    b.M, b.d, b.F = 16384 + 32, 8192, 8192  # 64 x 4 B per row: one row block past 4 MiB
+    assert lib.coda_block_fwd_noalloc(b, None) == UNSUPPORTED
+    assert b"static scratch" in lib.coda_last_error()
+    b.M = 0
+    assert lib.coda_block_fwd_noalloc(b, None) == 0  # nothing to do, nothing launched
+
+
 def test_fp8_host_validation(lib):
     INVALID, UNSUPPORTED = -1, -2
     good = _p(0x10000)
